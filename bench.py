@@ -1,0 +1,350 @@
+"""Benchmark of the decode-step MoE block on GB300.
+
+One step = one decode token (T = 1) through the 36-layer MoE stack of the
+sharded-shape workload: H=2048, 256 experts, top-8, I=128 per expert, shared
+expert I=128, fp16, weights ~N(0, 0.02), x ~N(0, 1).  Each layer has its own
+weights (405 MB, 14.6 GB in all, far above the 129 MB L2) and each step uses
+one of four pre-generated input sets, so routing differs from step to step.
+The 36 single-launch layer kernels of a step are captured in a CUDA graph
+(chained with programmatic dependent launch) and replayed; every layer still
+reads its input only after the previous layer's kernel has completed.
+
+Prints one JSON line.  ``--impl reference`` times the CPU oracle instead
+(single-threaded fp64, a bounded sample of the same workload).
+Multi-GPU (torchrun): every rank runs an independent replica ("replicas
+only": the T = 1 block does not shard); value = all ranks' tokens / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import moe_synth  # noqa: E402
+
+METRIC = "MoE decode layer µs & achieved HBM GB/s (% of GB300 peak) at T=1; tokens/s"
+NX = 4  # input sets rotated across steps
+
+
+def algorithmic_bytes(wl, T=1) -> int:
+    """Bytes one T=1 layer must move: router, the k selected experts' W13 and W2
+    rows, the shared expert (and gate vector), x in and out."""
+    H, E, k, I, Is = wl.hidden, wl.n_experts, wl.top_k, wl.inter, wl.shared_inter
+    n = E * H + k * 2 * I * H + k * H * I + 2 * Is * H + H * Is + (H if wl.has_shared_gate else 0)
+    return 2 * n + 2 * T * H * 2
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return ws, rank, local
+
+
+def reduce_max(v: float, ws: int) -> float:
+    if ws == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ oracle
+def oracle_sample(wl, layers, max_seconds, get_layer):
+    """Time the CPU oracle on (layer, token) samples of the workload: returns
+    (seconds, layers evaluated).  Inputs are copied to the host outside the
+    timed part; the oracle routes on the host and reads only the experts it
+    selects."""
+    import oracle
+    c = oracle.OracleCfg(wl.hidden, wl.n_experts, wl.top_k, wl.inter, wl.shared_inter, wl.dtype,
+                         wl.norm_topk, wl.has_shared_gate)
+    b = moe_synth.bits
+    spent, n = 0.0, 0
+    for l in range(layers):
+        g = get_layer(l)
+        x, wr = b(g["x"]), b(g["router_w"])
+        _, ids, _ = oracle.router(c, x[0], wr)
+        w13 = {int(e): b(g["w13"][int(e)]) for e in ids}
+        w2 = {int(e): b(g["w2"][int(e)]) for e in ids}
+        sh = (b(g["shared_w13"]), b(g["shared_w2"]), b(g["shared_gate_w"]))
+        del g
+        t0 = time.perf_counter()
+        oracle.moe_forward(c, x, wr, w13, w2, *sh)
+        spent += time.perf_counter() - t0
+        n += 1
+        if spent >= max_seconds:
+            break
+    return spent, n
+
+
+def run_reference(args, wl, ws_, rank):
+    if rank != 0:
+        return
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    budget = min(30.0, max(5.0, 0.002 * (args.steps + args.warmup)))
+    spent, n = oracle_sample(wl, wl.layers, budget, lambda l: moe_synth.make_layer(wl, l, 1, device=dev))
+    s_per_layer = spent / n
+    value = 1.0 / (s_per_layer * wl.layers)   # tokens/s through the 36-layer stack
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "impl": "reference", "n_gpus": args.gpus,
+        "steps": n, "warmup": 0, "ms_per_step": s_per_layer * wl.layers * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(wl),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{n} layers x 1 token of the workload, {spent:.1f} s of oracle time, "
+                                   f"scaled to the {wl.layers}-layer step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(wl):
+    return {"workload": f"{wl.name}: H={wl.hidden} E={wl.n_experts} top-{wl.top_k} I={wl.inter} "
+                        f"shared I={wl.shared_inter}{' +sigmoid gate' if wl.has_shared_gate else ''} "
+                        f"{'fp16' if wl.dtype == 1 else 'bf16'} T=1, {wl.layers} layers rotated",
+            "T": 1, "layers": wl.layers, "global_batch": 1, "seq_len": 1,
+            "parallelism": "replicas",
+            "l2": f"inputs larger than L2: {wl.layers} layers x {wl.layer_bytes() / 1e6:.0f} MB of weights, "
+                  f"{NX} input sets rotated per step"}
+
+
+# -------------------------------------------------------------------- ours
+def run_ours(args, wl, ws_n, rank, local):
+    import moe_decode_expert_gb300 as m
+
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    cfg = m.cfg_from_workload(wl)
+    L = wl.layers
+    H, k = wl.hidden, wl.top_k
+    layers = [moe_synth.make_layer(wl, l, 1, device=dev, weights_only=True) for l in range(L)]
+    xs = [[moe_synth.make_x(wl, l, 1, dev, seed_base=7919 * s) for l in range(L)] for s in range(NX)]
+    outs = torch.empty(L, 1, H, dtype=cfg.out_torch_dtype, device=dev)
+    ids = torch.empty(L, 1, k, dtype=torch.int32, device=dev)
+    wts = torch.empty(L, 1, k, dtype=torch.float32, device=dev)
+    ws = m.alloc_workspace(cfg, 1, dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(s):
+        for l in range(L):
+            g = layers[l]
+            m.moe_decode_forward(cfg, xs[s][l], g["router_w"], g["w13"], g["w2"], g["shared_w13"],
+                                 g["shared_w2"], g["shared_gate_w"], ids[l], wts[l], outs[l], ws, stream)
+
+    with torch.cuda.stream(stream):
+        for s in range(NX):
+            step(s)
+    torch.cuda.synchronize()
+    m.moe_query_status(ws, stream)
+    graphs = []
+    for s in range(NX):
+        gph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gph, stream=stream):
+            step(s)
+        graphs.append(gph)
+
+    K, W = args.steps, args.warmup
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            graphs[i % NX].replay()
+    torch.cuda.synchronize()
+    m.moe_query_status(ws, stream)
+
+    clocks = ClockSampler(local)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(ws_n)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(K):
+            graphs[i % NX].replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(ws_n)
+    ms = e0.elapsed_time(e1)
+    ms_max = reduce_max(ms, ws_n)
+    m.moe_query_status(ws, stream)
+
+    # ------------------------------------------------ end to end, host buffers
+    E2E_STEPS = max(5, min(200, K // 20))
+    xh = torch.empty(L, 1, H, dtype=cfg.torch_dtype, pin_memory=True)
+    xh.copy_(torch.stack([xs[0][l] for l in range(L)]).cpu())
+    xd = torch.empty(L, 1, H, dtype=cfg.torch_dtype, device=dev)
+    oh = torch.empty(L, 1, H, dtype=cfg.out_torch_dtype, pin_memory=True)
+    torch.cuda.synchronize()
+    barrier(ws_n)
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(E2E_STEPS):
+            xd.copy_(xh, non_blocking=True)
+            for l in range(L):
+                g = layers[l]
+                m.moe_decode_forward(cfg, xd[l], g["router_w"], g["w13"], g["w2"], g["shared_w13"],
+                                     g["shared_w2"], g["shared_gate_w"], ids[l], wts[l], outs[l], ws, stream)
+            oh.copy_(outs, non_blocking=True)
+            stream.synchronize()
+    e2e_s = reduce_max(time.perf_counter() - t0, ws_n)
+    m.moe_query_status(ws, stream)
+
+    # ----------------------------------------------------------- CPU oracle
+    cpu = None
+    if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
+        spent, n = oracle_sample(wl, L, args.cpu_seconds, lambda l: {**layers[l], "x": xs[0][l]})
+        cpu = {"value": 1.0 / (spent / n * L), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"{n} layers x 1 token of the workload ({spent:.1f} s single-threaded fp64), "
+                         f"scaled to the {L}-layer step"}
+
+    if rank != 0:
+        return
+    tokens = K * ws_n
+    value = tokens / (ms_max / 1e3)
+    us_layer = ms_max * 1e3 / (K * L)
+    alg = algorithmic_bytes(wl)
+    peak, peak_kind = measured_peaks()
+    achieved = alg / (us_layer * 1e-6) / 1e9
+    prof = os.path.join(ROOT, "profiles", f"decode_fused_kernel_{wl.name}.json")
+    traffic = None
+    if os.path.exists(prof):
+        with open(prof) as f:
+            pj = json.load(f)
+        traffic = pj.get("dram_bytes_per_launch")
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws_n, "steps": K, "warmup": W,
+        "ms_per_step": ms_max / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16" if wl.dtype == 1 else "bf16", "data": "synthetic (seeded N(0,0.02) weights, N(0,1) x)",
+        "config": config_of(wl),
+        "us_per_layer": us_layer,
+        "hbm_gbs": achieved,
+        "hbm_frac_of_peak": achieved / peak,
+        "kernels_per_layer": 1,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "kernel": "decode_fused_kernel",
+                     "algorithmic_bytes_per_launch": alg, "peak_kind": f"{peak_kind} (hbm_gbs)"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": E2E_STEPS * ws_n / e2e_s, "unit": "tokens/s",
+                "h2d_bytes_per_step": L * H * 2, "d2h_bytes_per_step": L * H * outs.element_size(),
+                "path": "moe_decode_forward per layer through the C ABI (no graph), pinned host x in, out back"},
+        "gpu_launches": K * L,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="sharded_decode",
+                    choices=["sharded_decode", "full_decode", "tiny"])
+    ap.add_argument("--layers", type=int, default=None)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    wl = moe_synth.workload(args.workload)
+    if args.layers:
+        wl = moe_synth.workload(args.workload, layers=args.layers)
+    ws_n, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, wl, ws_n, rank)
+    else:
+        run_ours(args, wl, ws_n, rank, local)
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

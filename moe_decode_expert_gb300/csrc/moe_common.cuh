@@ -1,0 +1,317 @@
+// moe_common.cuh — device helpers shared by the MoE kernels (sm_103a).
+//
+// Streaming weight loads, fp16/bf16 unpacking, warp reductions, the warp
+// top-k selector, bounded waits on the GPU global timer, the low-latency
+// (value, epoch) words CTAs exchange through global memory, mbarrier and
+// bulk-copy (TMA, untiled) wrappers, and programmatic-dependent-launch
+// controls.  Inline PTX only; no library kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+// ------------------------------------------------------------------ status
+// Device status codes recorded in the workspace control block (first wins).
+enum : uint32_t {
+  kDevOk = 0,
+  kDevTimeoutLogits = 1,  // router logits of another CTA never arrived
+  kDevTimeoutAct = 2,     // activations of another CTA never arrived
+  kDevTimeoutCopy = 3,    // a bulk copy never completed
+  kDevBadExpert = 4,      // an expert id outside [0, E)
+  kDevTimeoutTest = 5,    // the test hook's wait ran out (expected)
+};
+
+// Control block at offset 0 of every workspace (256 bytes).
+struct Control {
+  uint32_t status;     // first device-side error code, 0 = none
+  uint32_t detail;     // CTA (or token) that recorded it
+  uint32_t gen;        // epoch of the last single-launch decode on this workspace
+  uint32_t never_set;  // a flag no kernel writes (failure-path test)
+  uint32_t pad[60];
+};
+static_assert(sizeof(Control) == 256, "control block is 256 bytes");
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void report_error(Control* c, uint32_t code, uint32_t detail) {
+  if (atomicCAS(&c->status, 0u, code) == 0u) atomicExch(&c->detail, detail);
+}
+
+// ------------------------------------------------ programmatic dependent launch
+// Let the next kernel on the stream start launching (its CTAs then block in
+// their own pdl_wait until this grid has completed and flushed).
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until the preceding kernel on the stream has completed and its memory
+// operations are visible.  A no-op when launched without the PDL attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// --------------------------------------------------------------- loads
+// 16-byte streaming load of read-only weights: not kept in L1, with a 256-byte
+// L2 prefetch hint (consecutive lanes read consecutive 16-byte chunks).
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint4 ld_nc16(const void* p) {
+  uint4 r;
+  asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
+  return r;
+}
+
+// Two 2-byte floats packed in a 32-bit word -> two fp32 (exact).
+template <int DT>
+__device__ __forceinline__ float2 unpack2(uint32_t w) {
+  if constexpr (DT == MOE_BF16) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  } else {
+    __half2 h = *reinterpret_cast<__half2*>(&w);
+    return __half22float2(h);
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+  float2 a = unpack2<DT>(v.x), b = unpack2<DT>(v.y), c = unpack2<DT>(v.z), d = unpack2<DT>(v.w);
+  f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+  f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+}
+
+template <int DT>
+__device__ __forceinline__ float load_scalar(const void* base, size_t idx) {
+  const uint16_t b = reinterpret_cast<const uint16_t*>(base)[idx];
+  if constexpr (DT == MOE_BF16) return __uint_as_float(static_cast<uint32_t>(b) << 16);
+  else return __half2float(__ushort_as_half(b));
+}
+
+// Store one fp32 result in the output element type (round to nearest even).
+__device__ __forceinline__ void store_out(void* out, size_t idx, float v, int out_dtype) {
+  if (out_dtype == MOE_F32) {
+    reinterpret_cast<float*>(out)[idx] = v;
+  } else if (out_dtype == MOE_BF16) {
+    reinterpret_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
+  } else {
+    reinterpret_cast<__half*>(out)[idx] = __float2half_rn(v);
+  }
+}
+
+// ---------------------------------------------------------- reductions
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+__device__ __forceinline__ float sigmoid_f(float s) { return 1.0f / (1.0f + expf(-s)); }
+
+// Order-preserving map of a finite fp32 onto uint32 (larger float -> larger
+// key).  Every finite value (and -inf) maps above 0, so 0 can mark "taken".
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// Top-k of n <= 32*MAXM fp32 values held in shared memory, by (value desc,
+// index asc).  Called by all 32 lanes of one warp.  Lane l owns the
+// contiguous index range [l*m, l*m + m), so among lanes whose best keys tie,
+// the lowest lane holds the lowest index; within a lane a strict '>' scan
+// keeps the lowest index.  Writes out_ids[0..k) and out_vals[0..k).
+template <int MAXM>
+__device__ __forceinline__ void warp_topk(const float* vals, int n, int k, int* out_ids,
+                                          float* out_vals) {
+  const int lane = threadIdx.x & 31;
+  const int m = (n + 31) >> 5;
+  uint32_t key[MAXM];
+#pragma unroll
+  for (int s = 0; s < MAXM; ++s) {
+    const int idx = lane * m + s;
+    key[s] = (s < m && idx < n) ? order_key(vals[idx]) : 0u;
+  }
+  uint32_t bk = 0u;
+  int bs = -1;
+#pragma unroll
+  for (int s = 0; s < MAXM; ++s)
+    if (key[s] > bk) { bk = key[s]; bs = s; }
+  for (int r = 0; r < k; ++r) {
+    const uint32_t mx = __reduce_max_sync(0xffffffffu, bk);
+    const uint32_t ball = __ballot_sync(0xffffffffu, bs >= 0 && bk == mx);
+    const int winner = __ffs(ball) - 1;
+    if (lane == winner) {
+      const int idx = lane * m + bs;
+      out_ids[r] = idx;
+      out_vals[r] = vals[idx];
+#pragma unroll
+      for (int s = 0; s < MAXM; ++s)
+        if (s == bs) key[s] = 0u;
+      bk = 0u;
+      bs = -1;
+#pragma unroll
+      for (int s = 0; s < MAXM; ++s)
+        if (key[s] > bk) { bk = key[s]; bs = s; }
+    }
+    __syncwarp();
+  }
+}
+
+// Routing weights for the k selected logits (sel[0] is the largest).  With
+// norm_topk: softmax over the k selected logits, which equals the full
+// softmax renormalised over the k.  Without: exp(l - max) / sum over all n.
+// Called by one full warp; lane j < k writes w[j].
+__device__ __forceinline__ void warp_routing_weights(const float* all, int n, const float* sel,
+                                                     int k, int norm_topk, float* w) {
+  const int lane = threadIdx.x & 31;
+  const float mx = sel[0];
+  const float ej = lane < k ? expf(sel[lane] - mx) : 0.0f;
+  float z;
+  if (norm_topk) {
+    z = warp_sum(ej);
+  } else {
+    float part = 0.0f;
+    for (int e = lane; e < n; e += 32) part += expf(all[e] - mx);
+    z = warp_sum(part);
+  }
+  if (lane < k) w[lane] = ej / z;
+}
+
+// ----------------------------------------------- low-latency exchange words
+// A 64-bit word carrying an fp32 value (low half) and the launch epoch (high
+// half), written with one single-copy-atomic store.  A reader that sees the
+// current epoch in the high half also sees the value written with it, so one
+// load is both the flag check and the data read.
+__device__ __forceinline__ void ll_store(uint64_t* p, float v, uint32_t epoch) {
+  const uint64_t w = (static_cast<uint64_t>(epoch) << 32) | __float_as_uint(v);
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+// Two consecutive exchange words (16-byte aligned) in one vector load; each
+// 64-bit element is read single-copy atomically.  No "memory" clobber, so the
+// compiler may issue a batch of these before using any result.
+__device__ __forceinline__ ulonglong2 ll_load2(const uint64_t* p) {
+  ulonglong2 w;
+  asm volatile("ld.relaxed.gpu.global.v2.b64 {%0,%1}, [%2];" : "=l"(w.x), "=l"(w.y) : "l"(p));
+  return w;
+}
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Gather n exchange words of this epoch into dst (fp32).  `nthr` threads
+// cooperate, this one being `tid`; word pairs are read with 16-byte loads
+// (the word array is padded to an even length).  Up to 2*kLLBatch words per
+// thread are requested back to back, so the common case costs one L2 round
+// trip; words not yet published are re-polled until `deadline`.  Returns
+// false if words were still missing then.
+constexpr int kLLBatch = 16;
+__device__ __forceinline__ bool ll_gather(const uint64_t* src, float* dst, int n, int tid, int nthr,
+                                          uint32_t epoch, uint64_t deadline) {
+  const int npairs = (n + 1) >> 1;
+  for (int base = tid; base < npairs; base += nthr * kLLBatch) {
+    ulonglong2 w[kLLBatch];
+#pragma unroll
+    for (int u = 0; u < kLLBatch; ++u) {
+      const int q = base + u * nthr;
+      if (q < npairs) w[u] = ll_load2(src + 2 * q);
+    }
+    uint32_t missing = 0;
+#pragma unroll
+    for (int u = 0; u < kLLBatch; ++u) {
+      const int q = base + u * nthr;
+      if (q < npairs) {
+        const bool ok0 = static_cast<uint32_t>(w[u].x >> 32) == epoch;
+        const bool ok1 = 2 * q + 1 >= n || static_cast<uint32_t>(w[u].y >> 32) == epoch;
+        if (ok0 && ok1) {
+          dst[2 * q] = __uint_as_float(static_cast<uint32_t>(w[u].x));
+          if (2 * q + 1 < n) dst[2 * q + 1] = __uint_as_float(static_cast<uint32_t>(w[u].y));
+        } else {
+          missing |= 1u << u;
+        }
+      }
+    }
+    while (missing) {
+      if (global_ns() > deadline) return false;
+#pragma unroll
+      for (int u = 0; u < kLLBatch; ++u)
+        if (missing & (1u << u)) w[u] = ll_load2(src + 2 * (base + u * nthr));
+#pragma unroll
+      for (int u = 0; u < kLLBatch; ++u) {
+        if (missing & (1u << u)) {
+          const int q = base + u * nthr;
+          const bool ok0 = static_cast<uint32_t>(w[u].x >> 32) == epoch;
+          const bool ok1 = 2 * q + 1 >= n || static_cast<uint32_t>(w[u].y >> 32) == epoch;
+          if (ok0 && ok1) {
+            dst[2 * q] = __uint_as_float(static_cast<uint32_t>(w[u].x));
+            if (2 * q + 1 < n) dst[2 * q + 1] = __uint_as_float(static_cast<uint32_t>(w[u].y));
+            missing &= ~(1u << u);
+          }
+        }
+      }
+    }
+  }
+  return true;
+}
+
+// ------------------------------------------------- mbarrier + bulk copies
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for phase `parity` of `bar` to complete, or until `deadline`.
+__device__ __forceinline__ bool mbar_wait_until(uint64_t* bar, uint32_t parity, uint64_t deadline) {
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_ns() > deadline) return false;
+  }
+  return true;
+}
+// Untiled bulk copy global -> this CTA's shared memory, completing `bytes` of
+// transaction count on `bar`.  dst, src 16-byte aligned; bytes % 16 == 0.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+}  // namespace moe

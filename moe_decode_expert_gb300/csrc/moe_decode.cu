@@ -1,0 +1,391 @@
+// moe_decode.cu — the whole T = 1 decode MoE block in one kernel launch.
+//
+// What it computes ("BI-V100 inference work log", Parts 3, 4, 9, 10):
+// router GEMV + softmax + top-k, the direct-routed W13 GEMV that reads only
+// the selected experts' rows in place (W13[expert_ids[k], row, :]) with
+// SiluAndMul fused into it, the W2 GEMV W2[expert_ids[k], h, :] fused with
+// the routing-weighted sum, and the shared expert (gate_up, SiluAndMul, down,
+// optional sigmoid gate) fused into the same pass.
+//
+// How (GB300 design, not the pages' BI-V100 kernels): one CTA per SM, each
+// owning a slice of every phase, all phases in one launch.
+//   phase 1  routing-independent rows — router rows, the shared gate row and
+//            the shared expert's gate/up pairs — as warp-per-row dot products
+//            with 16-byte streaming loads issued before x lands in smem;
+//            results are published as (value, epoch) exchange words.
+//   phase 2  every CTA gathers the E logits (one L2 round trip when they are
+//            all published), and one warp ranks them (fp32, lower index wins
+//            ties) and forms the routing weights; no grid barrier and no
+//            second kernel.
+//   phase 3  thread 0 bulk-copies (TMA, untiled) the selected experts' W2
+//            rows of this CTA's output slice into smem while the warps
+//            compute this CTA's share of the k*I routed gate/up pairs
+//            (W13 rows streamed to registers), apply SiLU*up and publish act.
+//   phase 4  every CTA gathers all k*I + Is activations, waits for its W2
+//            rows, and computes its slice of out[h] = sum_j w_j (W2_j act_j)
+//            + g (Ws2 sact).
+// The two exchanges replace two kernel boundaries; each wait is bounded by
+// the GPU global timer and records an error instead of hanging.  The kernel
+// triggers programmatic dependent launch at entry so the next call on the
+// stream launches early and waits in its own prologue.
+
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+constexpr int kDecThreads = 256;
+constexpr int kDecWarps = kDecThreads / 32;
+constexpr int kChunks = 8;  // 16-byte chunks per lane per row kept in flight
+
+struct DecodeArgs {
+  const uint8_t* x;
+  const uint8_t* wr;
+  const uint8_t* w13;
+  const uint8_t* w2;
+  const uint8_t* sw13;
+  const uint8_t* sw2;
+  const uint8_t* swg;
+  int32_t* topk_ids;
+  float* topk_w;
+  void* out;
+  Control* ctrl;
+  uint64_t* ll_logits;
+  uint64_t* ll_act;
+  int H, E, k, I, Is, has_gate, norm_topk, out_dtype;
+  uint32_t off_lg, off_act, off_w2;
+  uint64_t timeout_ns;
+};
+
+// Up to two weight rows of H 2-byte elements, streamed to registers 16 bytes
+// per lane per chunk (lane-strided, so a warp reads 512 contiguous bytes per
+// instruction), then dotted with x held in shared memory as fp32.
+template <int DT>
+struct RowPair {
+  const uint8_t* r0;
+  const uint8_t* r1;
+  int two;   // 1: two rows, 0: one row
+  uint4 v0[kChunks], v1[kChunks];
+
+  __device__ __forceinline__ void issue(int base, int nch, int lane) {
+#pragma unroll
+    for (int t = 0; t < kChunks; ++t) {
+      const int c = base + lane + 32 * t;
+      const bool in = c < nch;
+      v0[t] = in ? ld_stream16(r0 + 16 * static_cast<size_t>(c)) : make_uint4(0, 0, 0, 0);
+      v1[t] = (in && two) ? ld_stream16(r1 + 16 * static_cast<size_t>(c)) : make_uint4(0, 0, 0, 0);
+    }
+  }
+
+  // Completes the dot products whose first batch was issued with issue(0).
+  __device__ __forceinline__ void finish(const float* xs, int nch, int lane, float& d0, float& d1) {
+    float a0 = 0.f, a1 = 0.f;
+    for (int base = 0; base < nch; base += 32 * kChunks) {
+      if (base) issue(base, nch, lane);
+#pragma unroll
+      for (int t = 0; t < kChunks; ++t) {
+        const int c = base + lane + 32 * t;
+        if (c < nch) {
+          const float4 xa = reinterpret_cast<const float4*>(xs)[2 * c];
+          const float4 xb = reinterpret_cast<const float4*>(xs)[2 * c + 1];
+          float f[8];
+          unpack8<DT>(v0[t], f);
+          a0 = fmaf(f[0], xa.x, a0); a0 = fmaf(f[1], xa.y, a0);
+          a0 = fmaf(f[2], xa.z, a0); a0 = fmaf(f[3], xa.w, a0);
+          a0 = fmaf(f[4], xb.x, a0); a0 = fmaf(f[5], xb.y, a0);
+          a0 = fmaf(f[6], xb.z, a0); a0 = fmaf(f[7], xb.w, a0);
+          if (two) {
+            unpack8<DT>(v1[t], f);
+            a1 = fmaf(f[0], xa.x, a1); a1 = fmaf(f[1], xa.y, a1);
+            a1 = fmaf(f[2], xa.z, a1); a1 = fmaf(f[3], xa.w, a1);
+            a1 = fmaf(f[4], xb.x, a1); a1 = fmaf(f[5], xb.y, a1);
+            a1 = fmaf(f[6], xb.z, a1); a1 = fmaf(f[7], xb.w, a1);
+          }
+        }
+      }
+    }
+    d0 = warp_sum(a0);
+    d1 = warp_sum(a1);
+  }
+};
+
+// Dot of one W2 row (n 2-byte elements in smem) with n fp32 activations,
+// lane-strided over 16-byte chunks; returns this lane's partial sum.
+template <int DT>
+__device__ __forceinline__ float smem_row_dot(const uint8_t* row, const float* act, int n, int lane) {
+  float acc = 0.f;
+  const int nch = n >> 3;
+  for (int c = lane; c < nch; c += 32) {
+    const uint4 v = *reinterpret_cast<const uint4*>(row + 16 * c);
+    const float4 xa = reinterpret_cast<const float4*>(act)[2 * c];
+    const float4 xb = reinterpret_cast<const float4*>(act)[2 * c + 1];
+    float f[8];
+    unpack8<DT>(v, f);
+    acc = fmaf(f[0], xa.x, acc); acc = fmaf(f[1], xa.y, acc);
+    acc = fmaf(f[2], xa.z, acc); acc = fmaf(f[3], xa.w, acc);
+    acc = fmaf(f[4], xb.x, acc); acc = fmaf(f[5], xb.y, acc);
+    acc = fmaf(f[6], xb.z, acc); acc = fmaf(f[7], xb.w, acc);
+  }
+  return acc;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kDecThreads, 2) decode_fused_kernel(const DecodeArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int s_ids[32];
+  __shared__ float s_sel[32];
+  __shared__ float s_w[32];
+  __shared__ float s_gate;
+  __shared__ uint32_t s_epoch;
+  __shared__ uint32_t s_fail;
+  __shared__ int s_second_arrive_done;
+
+  float* xs = reinterpret_cast<float*>(smem);
+  float* lg = reinterpret_cast<float*>(smem + a.off_lg);
+  float* acts = reinterpret_cast<float*>(smem + a.off_act);
+  uint8_t* w2s = smem + a.off_w2;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int cta = blockIdx.x, G = gridDim.x;
+  const int H = a.H, E = a.E, k = a.k, I = a.I, Is = a.Is;
+  const int h0 = static_cast<int>((static_cast<long long>(H) * cta) / G);
+  const int hn = static_cast<int>((static_cast<long long>(H) * (cta + 1)) / G) - h0;
+  const size_t rowb = static_cast<size_t>(H) * 2;
+  const int nch = H >> 3;
+
+  if (tid == 0) {
+    mbar_init(&bar, 2);
+    mbar_fence_init();
+    s_fail = 0;
+    s_second_arrive_done = 0;
+  }
+  pdl_launch_dependents();
+  __syncthreads();
+  pdl_wait();  // x (and anything else an earlier kernel wrote) is visible from here
+
+  // ---- phase 1: routing-independent rows; the first round's loads go out before x is staged
+  const int n1 = E + a.has_gate + Is;
+  int q = warp;
+  int u = q * G + cta;
+  RowPair<DT> rp;
+  auto setup_unit = [&](int uu) {
+    if (uu < E) {
+      rp.r0 = a.wr + static_cast<size_t>(uu) * rowb; rp.r1 = rp.r0; rp.two = 0;
+    } else if (uu < E + a.has_gate) {
+      rp.r0 = a.swg; rp.r1 = rp.r0; rp.two = 0;
+    } else {
+      const int i = uu - E - a.has_gate;
+      rp.r0 = a.sw13 + static_cast<size_t>(i) * rowb;
+      rp.r1 = a.sw13 + static_cast<size_t>(Is + i) * rowb;
+      rp.two = 1;
+    }
+  };
+  if (u < n1) { setup_unit(u); rp.issue(0, nch, lane); }
+
+  for (int c = tid; c < nch; c += kDecThreads) {
+    float f[8];
+    unpack8<DT>(ld_nc16(a.x + 16 * static_cast<size_t>(c)), f);
+    reinterpret_cast<float4*>(xs)[2 * c] = make_float4(f[0], f[1], f[2], f[3]);
+    reinterpret_cast<float4*>(xs)[2 * c + 1] = make_float4(f[4], f[5], f[6], f[7]);
+  }
+  if (tid == 0) {
+    uint32_t ep = ld_relaxed_u32(&a.ctrl->gen) + 1u;
+    s_epoch = ep ? ep : 1u;
+    if (Is > 0 && hn > 0) {  // shared expert's W2 rows of this CTA's slice
+      const uint32_t bytes = static_cast<uint32_t>(hn) * Is * 2;
+      mbar_arrive_expect_tx(&bar, bytes);
+      bulk_g2s(w2s + static_cast<size_t>(k) * hn * I * 2, a.sw2 + static_cast<size_t>(h0) * Is * 2, bytes, &bar);
+    } else {
+      mbar_arrive(&bar);
+    }
+  }
+  __syncthreads();
+  const uint32_t epoch = s_epoch;
+
+  while (u < n1) {
+    float d0, d1;
+    rp.finish(xs, nch, lane, d0, d1);
+    if (lane == 0) {
+      if (u < E + a.has_gate) ll_store(a.ll_logits + u, d0, epoch);
+      else ll_store(a.ll_act + static_cast<size_t>(k) * I + (u - E - a.has_gate), silu_f(d0) * d1, epoch);
+    }
+    q += kDecWarps;
+    u = q * G + cta;
+    if (u < n1) { setup_unit(u); rp.issue(0, nch, lane); }
+  }
+
+  // ---- phase 2: gather the logits, rank, weights (warp 0)
+  if (warp == 0) {
+    const int nl = E + a.has_gate;
+    const bool ok = ll_gather(a.ll_logits, lg, nl, lane, 32, epoch, global_ns() + a.timeout_ns);
+    if (__all_sync(0xffffffffu, ok)) {
+      __syncwarp();
+      if (E <= 256) warp_topk<8>(lg, E, k, s_ids, s_sel);
+      else warp_topk<32>(lg, E, k, s_ids, s_sel);
+      __syncwarp();
+      warp_routing_weights(lg, E, s_sel, k, a.norm_topk, s_w);
+      if (lane == 0) s_gate = a.has_gate ? sigmoid_f(lg[E]) : 1.0f;
+    } else if (lane == 0) {
+      s_fail = kDevTimeoutLogits;
+    }
+  }
+  __syncthreads();
+
+  if (!s_fail) {
+    // ---- phase 3: W2 rows of this CTA's slice (bulk copies), routed W13 pairs (registers)
+    if (tid == 0) {
+      if (hn > 0) {
+        const uint32_t bytes = static_cast<uint32_t>(hn) * I * 2;
+        mbar_arrive_expect_tx(&bar, bytes * k);
+        for (int j = 0; j < k; ++j)
+          bulk_g2s(w2s + static_cast<size_t>(j) * hn * I * 2,
+                   a.w2 + (static_cast<size_t>(s_ids[j]) * H + h0) * I * 2, bytes, &bar);
+      } else {
+        mbar_arrive(&bar);
+      }
+      s_second_arrive_done = 1;
+    }
+    if (cta == 0 && tid < k) {
+      a.topk_ids[tid] = s_ids[tid];
+      a.topk_w[tid] = s_w[tid];
+    }
+    const int P = k * I;
+    for (int qq = warp;; qq += kDecWarps) {
+      const int p = qq * G + cta;
+      if (p >= P) break;
+      const int j = p / I, i = p - j * I;
+      const size_t erow = static_cast<size_t>(s_ids[j]) * 2 * I;
+      rp.r0 = a.w13 + (erow + i) * rowb;
+      rp.r1 = a.w13 + (erow + I + i) * rowb;
+      rp.two = 1;
+      rp.issue(0, nch, lane);
+      float g, up;
+      rp.finish(xs, nch, lane, g, up);
+      if (lane == 0) ll_store(a.ll_act + p, silu_f(g) * up, epoch);
+    }
+
+    // ---- phase 4: all activations, this CTA's W2 rows, out slice
+    const bool ok = ll_gather(a.ll_act, acts, P + Is, tid, kDecThreads, epoch, global_ns() + a.timeout_ns);
+    if (!ok) s_fail = kDevTimeoutAct;
+    if (tid == 0 && !mbar_wait_until(&bar, 0, global_ns() + a.timeout_ns)) s_fail = kDevTimeoutCopy;
+    __syncthreads();
+    if (!s_fail) {
+      for (int r = warp; r < hn; r += kDecWarps) {
+        float acc = 0.f;
+        for (int j = 0; j < k; ++j) {
+          const uint8_t* row = w2s + (static_cast<size_t>(j) * hn + r) * I * 2;
+          acc = fmaf(s_w[j], smem_row_dot<DT>(row, acts + static_cast<size_t>(j) * I, I, lane), acc);
+        }
+        if (Is > 0) {
+          const uint8_t* row = w2s + (static_cast<size_t>(k) * hn * I + static_cast<size_t>(r) * Is) * 2;
+          acc = fmaf(s_gate, smem_row_dot<DT>(row, acts + P, Is, lane), acc);
+        }
+        acc = warp_sum(acc);
+        if (lane == 0) store_out(a.out, h0 + r, acc, a.out_dtype);
+      }
+      // Every CTA has read the epoch before publishing its activations and CTA 0
+      // has now seen all of them, so the next launch may use the next epoch.
+      if (cta == 0 && tid == 0) atomicExch(&a.ctrl->gen, epoch);
+      return;
+    }
+  }
+
+  // ---- failure path: record, let this CTA's own bulk copies land, bump the epoch
+  if (tid == 0) {
+    report_error(a.ctrl, s_fail, static_cast<uint32_t>(cta));
+    if (!s_second_arrive_done) mbar_arrive(&bar);
+    mbar_wait_until(&bar, 0, global_ns() + a.timeout_ns);
+    if (cta == 0) atomicExch(&a.ctrl->gen, epoch);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+int decode_grid(const moe_cfg_t& c) {
+  // One CTA per SM; never more CTAs than routed pairs, so that every CTA
+  // publishes at least one activation (the epoch hand-over relies on it).
+  const int pairs = c.top_k * c.inter;
+  int g = sm_count();
+  if (g > pairs) g = pairs;
+  return g < 1 ? 1 : g;
+}
+
+static void decode_smem_layout(const moe_cfg_t& c, int G, uint32_t& off_lg, uint32_t& off_act,
+                               uint32_t& off_w2, size_t& total) {
+  const size_t H = c.hidden, E = c.n_experts, k = c.top_k, I = c.inter, Is = c.shared_inter;
+  const size_t hn_max = (H + G - 1) / G;
+  size_t off = align_up(H * 4, 128);
+  off_lg = static_cast<uint32_t>(off);
+  off += align_up((E + 2) * 4, 128);
+  off_act = static_cast<uint32_t>(off);
+  off += align_up((k * I + Is + 2) * 4, 128);
+  off_w2 = static_cast<uint32_t>(off);
+  off += align_up(hn_max * (k * I + Is) * 2, 128);
+  total = off;
+}
+
+size_t decode_smem_bytes(const moe_cfg_t& c, int G) {
+  uint32_t a, b, d;
+  size_t t;
+  decode_smem_layout(c, G, a, b, d, t);
+  return t;
+}
+
+template <int DT>
+static moe_status_t launch_decode_dt(const DecodeArgs& args, int G, size_t smem, cudaStream_t st) {
+  static int configured_dev = -1;
+  static size_t configured_smem = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_dev != dev || configured_smem < smem) {
+    if (cudaFuncSetAttribute(decode_fused_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return check_launch("cudaFuncSetAttribute(decode)");
+    configured_dev = dev;
+    configured_smem = smem;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(G);
+  cfg.blockDim = dim3(kDecThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, decode_fused_kernel<DT>, args) != cudaSuccess)
+    return check_launch("decode_fused_kernel");
+  stat_kernels(1);
+  return MOE_OK;
+}
+
+moe_status_t launch_decode_fused(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws,
+                                 const WsLayout& L, cudaStream_t st) {
+  const int G = decode_grid(c);
+  DecodeArgs a;
+  a.x = static_cast<const uint8_t*>(p.x);
+  a.wr = static_cast<const uint8_t*>(p.router_w);
+  a.w13 = static_cast<const uint8_t*>(p.w13);
+  a.w2 = static_cast<const uint8_t*>(p.w2);
+  a.sw13 = static_cast<const uint8_t*>(p.shared_w13);
+  a.sw2 = static_cast<const uint8_t*>(p.shared_w2);
+  a.swg = static_cast<const uint8_t*>(p.shared_gate_w);
+  a.topk_ids = p.topk_ids;
+  a.topk_w = p.topk_w;
+  a.out = p.out;
+  a.ctrl = reinterpret_cast<Control*>(ws + L.ctrl);
+  a.ll_logits = reinterpret_cast<uint64_t*>(ws + L.ll_logits);
+  a.ll_act = reinterpret_cast<uint64_t*>(ws + L.ll_act);
+  a.H = c.hidden; a.E = c.n_experts; a.k = c.top_k; a.I = c.inter; a.Is = c.shared_inter;
+  a.has_gate = c.has_shared_gate; a.norm_topk = c.norm_topk; a.out_dtype = c.out_dtype;
+  size_t smem;
+  decode_smem_layout(c, G, a.off_lg, a.off_act, a.off_w2, smem);
+  a.timeout_ns = wait_timeout_ns();
+  if (smem > 227 * 1024)
+    return set_error(MOE_ERR_UNSUPPORTED, "decode: needs %zu B of shared memory per CTA (max 232448)", smem);
+  if (c.dtype == MOE_BF16) return launch_decode_dt<MOE_BF16>(a, G, smem, st);
+  return launch_decode_dt<MOE_F16>(a, G, smem, st);
+}
+
+}  // namespace moe

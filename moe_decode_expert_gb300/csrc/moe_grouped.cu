@@ -1,0 +1,324 @@
+// moe_grouped.cu — the MoE block for T > 1 tokens, grouped per expert.
+//
+// "Decode throughput analysis report", code-level profiling section: with
+// T >= 2 the pages' code fell into a prefill path that pulled the unique
+// expert ids to the host and looped over experts in Python; their fix
+// flattened the T*k (token, expert) pairs into batched products, and their
+// next step is a grouped GEMM.  Here the grouping happens on the device, with
+// no host synchronisation:
+//   group    counting sort of the T*k pairs by expert id (plus T pairs of
+//            the shared expert, filed as expert E), tile list of up to kTN
+//            pairs of one expert;
+//   w13      per (tile, block of gate/up pairs): the expert's W13 rows are
+//            streamed once per tile and dotted with the tile's tokens,
+//            SiLU(gate)*up -> act[pair] (fp32);
+//   w2       per (tile, block of output rows): y[pair, h] = weight(pair) *
+//            W2[e, h, :] . act[pair] (routing weight, or the shared gate);
+//   combine  out[t] = sum_j y[t*k + j] (+ y[shared pair of t]) in slot order.
+// Every output element is produced by one fixed sequence of fp32 operations,
+// so results do not depend on the order in which pairs were filed.
+
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+constexpr int kTN = 8;            // pairs (tokens) per tile
+constexpr int kGThreads = 256;
+constexpr int kGWarps = kGThreads / 32;
+constexpr int kPB = 32;           // gate/up pairs per w13 work item
+constexpr int kHB = 64;           // output rows per w2 work item
+
+// ------------------------------------------------------------- grouping
+// One CTA of 1024 threads.  counts/offsets/tiles live in the workspace.
+__global__ void __launch_bounds__(1024) group_kernel(const int32_t* __restrict__ ids, int T, int k, int E,
+                                                     int has_shared, int32_t* counts_out,
+                                                     int32_t* offsets, int32_t* perm, int32_t* tiles,
+                                                     Control* ctrl) {
+  __shared__ int32_t cnt[1025 + 1];
+  __shared__ int32_t cur[1025 + 1];
+  __shared__ int32_t tcnt[1025 + 1];
+  __shared__ int32_t wsum[32];
+  const int tid = threadIdx.x;
+  const int n = E + 1;  // experts + the shared expert
+  for (int e = tid; e < n; e += 1024) cnt[e] = 0;
+  __syncthreads();
+  const int np = T * k;
+  for (int p = tid; p < np; p += 1024) {
+    const int e = ids[p];
+    if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+    else report_error(ctrl, kDevBadExpert, static_cast<uint32_t>(p));
+  }
+  if (tid == 0) cnt[E] = has_shared ? T : 0;
+  __syncthreads();
+
+  // Exclusive scans of pair counts and tile counts (two elements per thread at most).
+  const int lane = tid & 31, warp = tid >> 5;
+  int c0 = 0, c1 = 0, t0 = 0, t1 = 0;
+  const int e0 = 2 * tid, e1 = 2 * tid + 1;
+  if (e0 < n) { c0 = cnt[e0]; t0 = (c0 + kTN - 1) / kTN; }
+  if (e1 < n) { c1 = cnt[e1]; t1 = (c1 + kTN - 1) / kTN; }
+  // pack pair and tile sums into one 64-bit scan value
+  unsigned long long v = (static_cast<unsigned long long>(c0 + c1) << 32) | static_cast<unsigned>(t0 + t1);
+  unsigned long long incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  __shared__ unsigned long long wtot[32];
+  if (lane == 31) wtot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    unsigned long long s = wtot[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    wtot[lane] = s;  // inclusive over warps
+  }
+  __syncthreads();
+  const unsigned long long before = incl - v + (warp ? wtot[warp - 1] : 0ull);
+  const int pb = static_cast<int>(before >> 32), tb = static_cast<int>(before & 0xffffffffu);
+  if (e0 < n) { cur[e0] = pb; tcnt[e0] = tb; }
+  if (e1 < n) { cur[e1] = pb + c0; tcnt[e1] = tb + t0; }
+  __syncthreads();
+  (void)wsum;
+  for (int e = tid; e < n; e += 1024) {
+    offsets[e] = cur[e];
+    counts_out[e] = cnt[e];
+    const int nt = (cnt[e] + kTN - 1) / kTN;
+    for (int tt = 0; tt < nt; ++tt) {
+      tiles[2 * (tcnt[e] + tt)] = e;
+      tiles[2 * (tcnt[e] + tt) + 1] = cur[e] + tt * kTN;
+    }
+  }
+  if (tid == 0) {
+    const unsigned long long tot = wtot[31];
+    offsets[n] = static_cast<int>(tot >> 32);
+    counts_out[n] = static_cast<int>(tot & 0xffffffffu);  // number of tiles
+  }
+  __syncthreads();
+  // File routed pairs (any order within an expert) and the shared pairs (in token order).
+  for (int p = tid; p < np; p += 1024) {
+    const int e = ids[p];
+    if (e >= 0 && e < E) perm[atomicAdd(&cur[e], 1)] = p;
+  }
+  if (has_shared)
+    for (int t = tid; t < T; t += 1024) perm[cur[E] + t] = np + t;
+}
+
+// Token of pair p (routed pairs t*k + j, then shared pairs T*k + t).
+__device__ __forceinline__ int pair_token(int p, int T, int k) { return p < T * k ? p / k : p - T * k; }
+
+// ----------------------------------------------------------- W13 + SiLU
+template <int DT>
+__global__ void __launch_bounds__(kGThreads) grouped_w13_kernel(
+    const uint8_t* __restrict__ x, const uint8_t* __restrict__ w13, const uint8_t* __restrict__ sw13,
+    const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets,
+    const int32_t* __restrict__ perm, const int32_t* __restrict__ tiles, int T, int H, int E, int k,
+    int I, int Is, int act_stride, float* __restrict__ act) {
+  extern __shared__ __align__(16) float xs[];   // [kTN][H] fp32
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_tiles = counts[E + 1];
+  const int Imax = I > Is ? I : Is;
+  const int npb = (Imax + kPB - 1) / kPB;
+  const size_t rowb = static_cast<size_t>(H) * 2;
+  const int nch = H >> 3;
+  for (int item = blockIdx.x; item < n_tiles * npb; item += gridDim.x) {
+    const int tile = item / npb, pb = item - tile * npb;
+    const int e = tiles[2 * tile], start = tiles[2 * tile + 1];
+    const int seg_end = offsets[e] + counts[e];
+    const int nt = min(kTN, seg_end - start);
+    const int ie = e == E ? Is : I;
+    if (pb * kPB >= ie) continue;
+    __syncthreads();  // previous item's readers of xs are done
+    for (int idx = threadIdx.x; idx < nt * nch; idx += kGThreads) {
+      const int r = idx / nch, c = idx - r * nch;
+      const int t = pair_token(perm[start + r], T, k);
+      float f[8];
+      unpack8<DT>(ld_nc16(x + static_cast<size_t>(t) * rowb + 16 * static_cast<size_t>(c)), f);
+      float4* d = reinterpret_cast<float4*>(xs + static_cast<size_t>(r) * H + 8 * c);
+      d[0] = make_float4(f[0], f[1], f[2], f[3]);
+      d[1] = make_float4(f[4], f[5], f[6], f[7]);
+    }
+    __syncthreads();
+    const uint8_t* base = e == E ? sw13 : w13 + static_cast<size_t>(e) * 2 * I * rowb;
+    for (int i = pb * kPB + warp; i < min(ie, (pb + 1) * kPB); i += kGWarps) {
+      const uint8_t* g_row = base + static_cast<size_t>(i) * rowb;
+      const uint8_t* u_row = base + static_cast<size_t>(ie + i) * rowb;
+      float ag[kTN], au[kTN];
+#pragma unroll
+      for (int r = 0; r < kTN; ++r) { ag[r] = 0.f; au[r] = 0.f; }
+      for (int c = lane; c < nch; c += 32) {
+        float fg[8], fu[8];
+        unpack8<DT>(ld_stream16(g_row + 16 * static_cast<size_t>(c)), fg);
+        unpack8<DT>(ld_stream16(u_row + 16 * static_cast<size_t>(c)), fu);
+#pragma unroll
+        for (int r = 0; r < kTN; ++r) {
+          if (r < nt) {
+            const float4 xa = reinterpret_cast<const float4*>(xs + static_cast<size_t>(r) * H)[2 * c];
+            const float4 xb = reinterpret_cast<const float4*>(xs + static_cast<size_t>(r) * H)[2 * c + 1];
+            const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              ag[r] = fmaf(fg[q], xv[q], ag[r]);
+              au[r] = fmaf(fu[q], xv[q], au[r]);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < kTN; ++r) {
+        const float g = warp_sum(ag[r]);
+        const float u = warp_sum(au[r]);
+        if (lane == 0 && r < nt) act[static_cast<size_t>(perm[start + r]) * act_stride + i] = silu_f(g) * u;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------ W2 + pair weight
+template <int DT>
+__global__ void __launch_bounds__(kGThreads) grouped_w2_kernel(
+    const uint8_t* __restrict__ w2, const uint8_t* __restrict__ sw2, const int32_t* __restrict__ counts,
+    const int32_t* __restrict__ offsets, const int32_t* __restrict__ perm,
+    const int32_t* __restrict__ tiles, const float* __restrict__ topk_w,
+    const float* __restrict__ gate_logits, int gate_stride, int has_gate, int T, int H, int E, int k,
+    int I, int Is, int act_stride, const float* __restrict__ act, float* __restrict__ y) {
+  extern __shared__ __align__(16) float as[];   // [kTN][Imax] fp32
+  __shared__ float s_wt[kTN];
+  __shared__ int s_pair[kTN];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_tiles = counts[E + 1];
+  const int nhb = (H + kHB - 1) / kHB;
+  for (int item = blockIdx.x; item < n_tiles * nhb; item += gridDim.x) {
+    const int tile = item / nhb, hb = item - tile * nhb;
+    const int e = tiles[2 * tile], start = tiles[2 * tile + 1];
+    const int seg_end = offsets[e] + counts[e];
+    const int nt = min(kTN, seg_end - start);
+    const int ie = e == E ? Is : I;
+    __syncthreads();
+    if (threadIdx.x < nt) {
+      const int p = perm[start + threadIdx.x];
+      s_pair[threadIdx.x] = p;
+      float wt;
+      if (p < T * k) wt = topk_w[p];
+      else wt = has_gate ? sigmoid_f(gate_logits[static_cast<size_t>(p - T * k) * gate_stride + E]) : 1.0f;
+      s_wt[threadIdx.x] = wt;
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < nt * (ie >> 2); idx += kGThreads) {
+      const int r = idx / (ie >> 2), c = idx - r * (ie >> 2);
+      reinterpret_cast<float4*>(as + static_cast<size_t>(r) * ie)[c] =
+          reinterpret_cast<const float4*>(act + static_cast<size_t>(s_pair[r]) * act_stride)[c];
+    }
+    __syncthreads();
+    const uint8_t* base = e == E ? sw2 : w2 + static_cast<size_t>(e) * H * I * 2;
+    const int nch = ie >> 3;
+    for (int h = hb * kHB + warp; h < min(H, (hb + 1) * kHB); h += kGWarps) {
+      const uint8_t* row = base + static_cast<size_t>(h) * ie * 2;
+      float acc[kTN];
+#pragma unroll
+      for (int r = 0; r < kTN; ++r) acc[r] = 0.f;
+      for (int c = lane; c < nch; c += 32) {
+        float f[8];
+        unpack8<DT>(ld_stream16(row + 16 * static_cast<size_t>(c)), f);
+#pragma unroll
+        for (int r = 0; r < kTN; ++r) {
+          if (r < nt) {
+            const float4 xa = reinterpret_cast<const float4*>(as + static_cast<size_t>(r) * ie)[2 * c];
+            const float4 xb = reinterpret_cast<const float4*>(as + static_cast<size_t>(r) * ie)[2 * c + 1];
+            const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[r] = fmaf(f[q], xv[q], acc[r]);
+          }
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < kTN; ++r) {
+        const float s = warp_sum(acc[r]);
+        if (lane == 0 && r < nt) y[static_cast<size_t>(s_pair[r]) * H + h] = s_wt[r] * s;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- combine
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, int T, int H, int k,
+                                                      int has_shared, void* out, int out_dtype) {
+  const size_t n = static_cast<size_t>(T) * H;
+  for (size_t idx = blockIdx.x * 256ull + threadIdx.x; idx < n; idx += static_cast<size_t>(gridDim.x) * 256) {
+    const size_t t = idx / H, h = idx - t * H;
+    float acc = 0.f;
+    for (int j = 0; j < k; ++j) acc += y[(t * k + j) * H + h];
+    if (has_shared) acc += y[(static_cast<size_t>(T) * k + t) * H + h];
+    store_out(out, idx, acc, out_dtype);
+  }
+}
+
+moe_status_t launch_grouped(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws, const WsLayout& L,
+                            int32_t T, cudaStream_t st) {
+  const int H = c.hidden, E = c.n_experts, k = c.top_k, I = c.inter, Is = c.shared_inter;
+  Control* ctrl = reinterpret_cast<Control*>(ws + L.ctrl);
+  if (moe_status_t s = launch_router(c, p.x, p.router_w, p.shared_gate_w, T, p.topk_ids, p.topk_w,
+                                     nullptr, ws, L, st))
+    return s;
+  int32_t* counts = reinterpret_cast<int32_t*>(ws + L.g_counts);
+  int32_t* offsets = reinterpret_cast<int32_t*>(ws + L.g_offsets);
+  int32_t* perm = reinterpret_cast<int32_t*>(ws + L.g_perm);
+  int32_t* tiles = reinterpret_cast<int32_t*>(ws + L.g_tiles);
+  float* act = reinterpret_cast<float*>(ws + L.g_act);
+  float* y = reinterpret_cast<float*>(ws + L.g_y);
+  const float* glog = reinterpret_cast<const float*>(ws + L.r_logits);
+  const int gate_stride = c.has_shared_gate ? E + 1 : E;
+  const int Imax = I > Is ? I : Is;
+
+  group_kernel<<<1, 1024, 0, st>>>(p.topk_ids, T, k, E, Is > 0, counts, offsets, perm, tiles, ctrl);
+  if (moe_status_t s = check_launch("group_kernel")) return s;
+
+  const int sms = sm_count();
+  const size_t smem13 = static_cast<size_t>(kTN) * H * 4;
+  const size_t smem2 = static_cast<size_t>(kTN) * Imax * 4;
+  if (smem13 > 227 * 1024 || smem2 > 227 * 1024)
+    return set_error(MOE_ERR_UNSUPPORTED, "grouped: hidden=%d or inter=%d too large for one tile", H, Imax);
+  const int npb = (Imax + kPB - 1) / kPB;
+  const int nhb = (H + kHB - 1) / kHB;
+  const long long items13 = L.max_tiles * npb, items2 = L.max_tiles * nhb;
+  const int g13 = static_cast<int>(items13 < sms * 8LL ? items13 : sms * 8LL);
+  const int g2 = static_cast<int>(items2 < sms * 8LL ? items2 : sms * 8LL);
+  const uint8_t* x = static_cast<const uint8_t*>(p.x);
+  if (c.dtype == MOE_BF16) {
+    cudaFuncSetAttribute(grouped_w13_kernel<MOE_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem13);
+    grouped_w13_kernel<MOE_BF16><<<g13, kGThreads, smem13, st>>>(
+        x, static_cast<const uint8_t*>(p.w13), static_cast<const uint8_t*>(p.shared_w13), counts, offsets,
+        perm, tiles, T, H, E, k, I, Is, Imax, act);
+  } else {
+    cudaFuncSetAttribute(grouped_w13_kernel<MOE_F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem13);
+    grouped_w13_kernel<MOE_F16><<<g13, kGThreads, smem13, st>>>(
+        x, static_cast<const uint8_t*>(p.w13), static_cast<const uint8_t*>(p.shared_w13), counts, offsets,
+        perm, tiles, T, H, E, k, I, Is, Imax, act);
+  }
+  if (moe_status_t s = check_launch("grouped_w13_kernel")) return s;
+  if (c.dtype == MOE_BF16) {
+    cudaFuncSetAttribute(grouped_w2_kernel<MOE_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
+    grouped_w2_kernel<MOE_BF16><<<g2, kGThreads, smem2, st>>>(
+        static_cast<const uint8_t*>(p.w2), static_cast<const uint8_t*>(p.shared_w2), counts, offsets, perm,
+        tiles, p.topk_w, glog, gate_stride, c.has_shared_gate, T, H, E, k, I, Is, Imax, act, y);
+  } else {
+    cudaFuncSetAttribute(grouped_w2_kernel<MOE_F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
+    grouped_w2_kernel<MOE_F16><<<g2, kGThreads, smem2, st>>>(
+        static_cast<const uint8_t*>(p.w2), static_cast<const uint8_t*>(p.shared_w2), counts, offsets, perm,
+        tiles, p.topk_w, glog, gate_stride, c.has_shared_gate, T, H, E, k, I, Is, Imax, act, y);
+  }
+  if (moe_status_t s = check_launch("grouped_w2_kernel")) return s;
+  const long long n = static_cast<long long>(T) * H;
+  const int gc = static_cast<int>((n + 255) / 256 < sms * 16LL ? (n + 255) / 256 : sms * 16LL);
+  combine_kernel<<<gc, 256, 0, st>>>(y, T, H, k, Is > 0, p.out, c.out_dtype);
+  if (moe_status_t s = check_launch("combine_kernel")) return s;
+  stat_kernels(4);
+  return MOE_OK;
+}
+
+}  // namespace moe

@@ -1,0 +1,81 @@
+// moe_internal.h — host-side plumbing shared by the library's translation
+// units: workspace layout, launch helpers, error reporting and counters.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+constexpr size_t kWsAlign = 256;
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Byte offsets of every region of one workspace, for `T` tokens of a cfg.
+struct WsLayout {
+  size_t ctrl = 0;        // Control block, 256 B
+  // single-launch decode (T == 1): exchange words between CTAs
+  size_t ll_logits = 0;   // (E + 1) words of 8 B, padded to even
+  size_t ll_act = 0;      // (k*I + Is) words
+  // router for T tokens
+  size_t r_logits = 0;    // [T, E + 1] fp32 (column E: shared-gate logit)
+  // grouped path (T > 1)
+  size_t g_counts = 0;    // (E + 2) int32: tokens per expert (E = shared)
+  size_t g_offsets = 0;   // (E + 2) int32: exclusive prefix of counts
+  size_t g_perm = 0;      // [P] int32: pair ids grouped by expert
+  size_t g_tiles = 0;     // [max_tiles + 1] int32 x2: (expert, first row) per tile
+  size_t g_act = 0;       // [P, max(I, Is)] fp32
+  size_t g_y = 0;         // [P, H] fp32 weighted expert outputs
+  size_t total = 0;
+  int64_t pairs = 0;      // P = T*k + (Is ? T : 0)
+  int64_t max_tiles = 0;
+};
+
+WsLayout ws_layout(const moe_cfg_t& c, int32_t T);
+
+// Host-side error recording (thread-local text + code).
+moe_status_t set_error(moe_status_t code, const char* fmt, ...);
+moe_status_t check_launch(const char* what);
+
+// Process-wide counters.
+void stat_decode();
+void stat_router();
+void stat_grouped();
+void stat_kernels(uint64_t n);
+
+// Device properties cached per device.
+int sm_count();
+uint64_t wait_timeout_ns();
+
+// Pointers of one MoE block call.
+struct BlockPtrs {
+  const void* x;
+  const void* router_w;
+  const void* w13;
+  const void* w2;
+  const void* shared_w13;
+  const void* shared_w2;
+  const void* shared_gate_w;
+  int32_t* topk_ids;
+  float* topk_w;
+  void* out;
+};
+
+// Kernel launchers (each returns MOE_OK or a host-side error).
+moe_status_t launch_decode_fused(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws,
+                                 const WsLayout& L, cudaStream_t st);
+moe_status_t launch_router(const moe_cfg_t& c, const void* x, const void* router_w,
+                           const void* shared_gate_w, int32_t T, int32_t* ids, float* w,
+                           float* logits_out, uint8_t* ws, const WsLayout& L, cudaStream_t st);
+moe_status_t launch_grouped(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws, const WsLayout& L,
+                            int32_t T, cudaStream_t st);
+moe_status_t launch_wait_test(uint8_t* ws, cudaStream_t st);
+
+// Grid size of the single-launch decode kernel for cfg c.
+int decode_grid(const moe_cfg_t& c);
+// Dynamic shared memory of that kernel (bytes) for grid G.
+size_t decode_smem_bytes(const moe_cfg_t& c, int G);
+
+}  // namespace moe
