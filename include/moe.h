@@ -96,8 +96,14 @@ typedef struct moe_cfg {
   int32_t norm_topk;       /* 1: renormalise the k weights to sum 1; 0: keep
                               the full-softmax probabilities                    */
   int32_t has_shared_gate; /* 1: shared output scaled by sigmoid(x . wg)       */
-  int32_t flags;           /* reserved, must be 0                              */
+  int32_t flags;           /* 0, or one MOE_FLAG_GROUPED_* bit (T > 1 path)    */
 } moe_cfg_t;
+
+/* cfg->flags bits selecting the T > 1 path.  With neither bit the library
+ * uses the CUDA-core grouped kernels. */
+#define MOE_FLAG_GROUPED_SIMT 1  /* T > 1 on the CUDA-core grouped kernels      */
+#define MOE_FLAG_GROUPED_TC 2    /* T > 1 on the tcgen05 grouped kernels;
+                                    MOE_ERR_UNSUPPORTED if the shape does not allow it */
 
 /* Caller-owned routing outputs, [T, k] each (device memory). */
 typedef struct moe_topk {
@@ -109,7 +115,8 @@ typedef struct moe_topk {
 typedef struct moe_stats {
   uint64_t decode_fused_calls;   /* T == 1 single-launch decode kernel          */
   uint64_t router_calls;         /* moe_router_topk                            */
-  uint64_t grouped_calls;        /* T > 1 grouped path                         */
+  uint64_t grouped_calls;        /* T > 1 grouped path (either kind)            */
+  uint64_t grouped_tc_calls;     /* ... of which on the tcgen05 kernels         */
   uint64_t kernels_launched;     /* every kernel this library enqueued          */
 } moe_stats_t;
 

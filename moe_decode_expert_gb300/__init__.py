@@ -51,7 +51,11 @@ class moe_topk_t(ctypes.Structure):
 
 class moe_stats_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in ("decode_fused_calls", "router_calls", "grouped_calls",
-                                               "kernels_launched")]
+                                               "grouped_tc_calls", "kernels_launched")]
+
+
+MOE_FLAG_GROUPED_SIMT = 1
+MOE_FLAG_GROUPED_TC = 2
 
 
 @dataclass(frozen=True)
@@ -65,11 +69,12 @@ class MoeCfg:
     out_dtype: int | None = None
     norm_topk: int = 1
     has_shared_gate: int = 0
+    flags: int = 0
 
     def c(self) -> moe_cfg_t:
         return moe_cfg_t(self.hidden, self.n_experts, self.top_k, self.inter, self.shared_inter, self.dtype,
                          self.dtype if self.out_dtype is None else self.out_dtype, self.norm_topk,
-                         self.has_shared_gate, 0)
+                         self.has_shared_gate, self.flags)
 
     @property
     def torch_dtype(self):
@@ -254,7 +259,7 @@ def moe_grouped_forward(cfg: MoeCfg, x, router_w, w13, w2, shared_w13, shared_w2
     _check(_load().moe_grouped_forward(ctypes.byref(c), *args, _ptr(ws), ws.numel(), T, _stream(stream)))
 
 
-def cfg_from_workload(wl, out_dtype=None) -> MoeCfg:
+def cfg_from_workload(wl, out_dtype=None, flags=0) -> MoeCfg:
     """MoeCfg for a synthetic workload description (moe_synth.Workload)."""
     return MoeCfg(wl.hidden, wl.n_experts, wl.top_k, wl.inter, wl.shared_inter, wl.dtype, out_dtype,
-                  wl.norm_topk, wl.has_shared_gate)
+                  wl.norm_topk, wl.has_shared_gate, flags)

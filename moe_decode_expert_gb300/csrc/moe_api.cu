@@ -30,10 +30,11 @@ moe_status_t check_launch(const char* what) {
 }
 
 // ---------------------------------------------------------------- counters
-static std::atomic<uint64_t> g_decode{0}, g_router{0}, g_grouped{0}, g_kernels{0};
+static std::atomic<uint64_t> g_decode{0}, g_router{0}, g_grouped{0}, g_grouped_tc{0}, g_kernels{0};
 void stat_decode() { g_decode.fetch_add(1, std::memory_order_relaxed); }
 void stat_router() { g_router.fetch_add(1, std::memory_order_relaxed); }
 void stat_grouped() { g_grouped.fetch_add(1, std::memory_order_relaxed); }
+void stat_grouped_tc() { g_grouped_tc.fetch_add(1, std::memory_order_relaxed); }
 void stat_kernels(uint64_t n) { g_kernels.fetch_add(n, std::memory_order_relaxed); }
 
 // ------------------------------------------------------------ device facts
@@ -84,6 +85,27 @@ WsLayout ws_layout(const moe_cfg_t& c, int32_t T) {
     off = align_up(off + static_cast<size_t>(P) * (I > Is ? I : Is) * 4, kWsAlign);
     L.g_y = off;
     off = align_up(off + static_cast<size_t>(P) * H * 4, kWsAlign);
+    if (tc_shape_ok(c)) {
+      const int64_t N = tc_tile_n(c, T);
+      const int64_t nt_routed = (T * k + N - 1) / N + E;
+      const int64_t nt_shared = Is > 0 ? (T + N - 1) / N : 0;
+      L.tc_n = static_cast<int>(N);
+      L.tc_max13 = nt_routed * (I / 64) + nt_shared * (Is / 64);
+      L.tc_max2 = (nt_routed + nt_shared) * (H / 128);
+      L.tc_sched = off;
+      off = align_up(off + 16, kWsAlign);
+      L.tc_tiles13 = off;
+      off = align_up(off + static_cast<size_t>(L.tc_max13) * 16, kWsAlign);
+      L.tc_tiles2 = off;
+      off = align_up(off + static_cast<size_t>(L.tc_max2) * 16, kWsAlign);
+      L.tc_xs = off;
+      off = align_up(off + static_cast<size_t>(P) * H * 2, kWsAlign);
+      const int64_t Imax = I > Is ? I : Is;
+      L.tc_act_hi = off;
+      off = align_up(off + static_cast<size_t>(P) * Imax * 2, kWsAlign);
+      L.tc_act_lo = off;
+      off = align_up(off + static_cast<size_t>(P) * Imax * 2, kWsAlign);
+    }
   }
   L.total = off;
   return L;
@@ -105,7 +127,10 @@ static moe_status_t check_cfg(const moe_cfg_t* c) {
     return set_error(MOE_ERR_INVALID_ARG, "cfg: has_shared_gate is 0 or 1");
   if (c->has_shared_gate && c->shared_inter == 0)
     return set_error(MOE_ERR_INVALID_ARG, "cfg: a shared gate needs a shared expert");
-  if (c->flags != 0) return set_error(MOE_ERR_INVALID_ARG, "cfg: flags must be 0");
+  if (c->flags & ~(MOE_FLAG_GROUPED_SIMT | MOE_FLAG_GROUPED_TC))
+    return set_error(MOE_ERR_INVALID_ARG, "cfg: unknown flag bits");
+  if ((c->flags & MOE_FLAG_GROUPED_SIMT) && (c->flags & MOE_FLAG_GROUPED_TC))
+    return set_error(MOE_ERR_INVALID_ARG, "cfg: MOE_FLAG_GROUPED_SIMT and MOE_FLAG_GROUPED_TC exclude each other");
   if (c->hidden % 8 || c->inter % 8 || c->shared_inter % 8)
     return set_error(MOE_ERR_UNSUPPORTED, "cfg: hidden, inter and shared_inter must be multiples of 8");
   if (c->top_k > 32 || c->top_k > c->n_experts)
@@ -279,6 +304,7 @@ moe_status_t moe_get_stats(moe_stats_t* stats) {
   stats->decode_fused_calls = g_decode.load();
   stats->router_calls = g_router.load();
   stats->grouped_calls = g_grouped.load();
+  stats->grouped_tc_calls = g_grouped_tc.load();
   stats->kernels_launched = g_kernels.load();
   return MOE_OK;
 }
@@ -287,6 +313,7 @@ void moe_reset_stats(void) {
   g_decode = 0;
   g_router = 0;
   g_grouped = 0;
+  g_grouped_tc = 0;
   g_kernels = 0;
 }
 

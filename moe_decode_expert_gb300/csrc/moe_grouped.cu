@@ -279,40 +279,49 @@ moe_status_t launch_grouped(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws,
   if (moe_status_t s = check_launch("group_kernel")) return s;
 
   const int sms = sm_count();
-  const size_t smem13 = static_cast<size_t>(kTN) * H * 4;
-  const size_t smem2 = static_cast<size_t>(kTN) * Imax * 4;
-  if (smem13 > 227 * 1024 || smem2 > 227 * 1024)
-    return set_error(MOE_ERR_UNSUPPORTED, "grouped: hidden=%d or inter=%d too large for one tile", H, Imax);
-  const int npb = (Imax + kPB - 1) / kPB;
-  const int nhb = (H + kHB - 1) / kHB;
-  const long long items13 = L.max_tiles * npb, items2 = L.max_tiles * nhb;
-  const int g13 = static_cast<int>(items13 < sms * 8LL ? items13 : sms * 8LL);
-  const int g2 = static_cast<int>(items2 < sms * 8LL ? items2 : sms * 8LL);
-  const uint8_t* x = static_cast<const uint8_t*>(p.x);
-  if (c.dtype == MOE_BF16) {
-    cudaFuncSetAttribute(grouped_w13_kernel<MOE_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem13);
-    grouped_w13_kernel<MOE_BF16><<<g13, kGThreads, smem13, st>>>(
-        x, static_cast<const uint8_t*>(p.w13), static_cast<const uint8_t*>(p.shared_w13), counts, offsets,
-        perm, tiles, T, H, E, k, I, Is, Imax, act);
+  const bool use_tc = (c.flags & MOE_FLAG_GROUPED_TC) && L.tc_n > 0 && tc_path_supported(c);
+  if ((c.flags & MOE_FLAG_GROUPED_TC) && !use_tc)
+    return set_error(MOE_ERR_UNSUPPORTED, "grouped: the tensor-core path needs bf16, H %% 128 == 0, "
+                                          "I and Is multiples of 64 and the TMA encoder");
+  if (use_tc) {
+    if (moe_status_t s = launch_tc_passes(c, p, ws, L, T, st)) return s;
+    stat_grouped_tc();
   } else {
-    cudaFuncSetAttribute(grouped_w13_kernel<MOE_F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem13);
-    grouped_w13_kernel<MOE_F16><<<g13, kGThreads, smem13, st>>>(
-        x, static_cast<const uint8_t*>(p.w13), static_cast<const uint8_t*>(p.shared_w13), counts, offsets,
-        perm, tiles, T, H, E, k, I, Is, Imax, act);
+    const size_t smem13 = static_cast<size_t>(kTN) * H * 4;
+    const size_t smem2 = static_cast<size_t>(kTN) * Imax * 4;
+    if (smem13 > 227 * 1024 || smem2 > 227 * 1024)
+      return set_error(MOE_ERR_UNSUPPORTED, "grouped: hidden=%d or inter=%d too large for one tile", H, Imax);
+    const int npb = (Imax + kPB - 1) / kPB;
+    const int nhb = (H + kHB - 1) / kHB;
+    const long long items13 = L.max_tiles * npb, items2 = L.max_tiles * nhb;
+    const int g13 = static_cast<int>(items13 < sms * 8LL ? items13 : sms * 8LL);
+    const int g2 = static_cast<int>(items2 < sms * 8LL ? items2 : sms * 8LL);
+    const uint8_t* x = static_cast<const uint8_t*>(p.x);
+    if (c.dtype == MOE_BF16) {
+      cudaFuncSetAttribute(grouped_w13_kernel<MOE_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem13);
+      grouped_w13_kernel<MOE_BF16><<<g13, kGThreads, smem13, st>>>(
+          x, static_cast<const uint8_t*>(p.w13), static_cast<const uint8_t*>(p.shared_w13), counts, offsets,
+          perm, tiles, T, H, E, k, I, Is, Imax, act);
+    } else {
+      cudaFuncSetAttribute(grouped_w13_kernel<MOE_F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem13);
+      grouped_w13_kernel<MOE_F16><<<g13, kGThreads, smem13, st>>>(
+          x, static_cast<const uint8_t*>(p.w13), static_cast<const uint8_t*>(p.shared_w13), counts, offsets,
+          perm, tiles, T, H, E, k, I, Is, Imax, act);
+    }
+    if (moe_status_t s = check_launch("grouped_w13_kernel")) return s;
+    if (c.dtype == MOE_BF16) {
+      cudaFuncSetAttribute(grouped_w2_kernel<MOE_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
+      grouped_w2_kernel<MOE_BF16><<<g2, kGThreads, smem2, st>>>(
+          static_cast<const uint8_t*>(p.w2), static_cast<const uint8_t*>(p.shared_w2), counts, offsets, perm,
+          tiles, p.topk_w, glog, gate_stride, c.has_shared_gate, T, H, E, k, I, Is, Imax, act, y);
+    } else {
+      cudaFuncSetAttribute(grouped_w2_kernel<MOE_F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
+      grouped_w2_kernel<MOE_F16><<<g2, kGThreads, smem2, st>>>(
+          static_cast<const uint8_t*>(p.w2), static_cast<const uint8_t*>(p.shared_w2), counts, offsets, perm,
+          tiles, p.topk_w, glog, gate_stride, c.has_shared_gate, T, H, E, k, I, Is, Imax, act, y);
+    }
+    if (moe_status_t s = check_launch("grouped_w2_kernel")) return s;
   }
-  if (moe_status_t s = check_launch("grouped_w13_kernel")) return s;
-  if (c.dtype == MOE_BF16) {
-    cudaFuncSetAttribute(grouped_w2_kernel<MOE_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
-    grouped_w2_kernel<MOE_BF16><<<g2, kGThreads, smem2, st>>>(
-        static_cast<const uint8_t*>(p.w2), static_cast<const uint8_t*>(p.shared_w2), counts, offsets, perm,
-        tiles, p.topk_w, glog, gate_stride, c.has_shared_gate, T, H, E, k, I, Is, Imax, act, y);
-  } else {
-    cudaFuncSetAttribute(grouped_w2_kernel<MOE_F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
-    grouped_w2_kernel<MOE_F16><<<g2, kGThreads, smem2, st>>>(
-        static_cast<const uint8_t*>(p.w2), static_cast<const uint8_t*>(p.shared_w2), counts, offsets, perm,
-        tiles, p.topk_w, glog, gate_stride, c.has_shared_gate, T, H, E, k, I, Is, Imax, act, y);
-  }
-  if (moe_status_t s = check_launch("grouped_w2_kernel")) return s;
   const long long n = static_cast<long long>(T) * H;
   const int gc = static_cast<int>((n + 255) / 256 < sms * 16LL ? (n + 255) / 256 : sms * 16LL);
   combine_kernel<<<gc, 256, 0, st>>>(y, T, H, k, Is > 0, p.out, c.out_dtype);

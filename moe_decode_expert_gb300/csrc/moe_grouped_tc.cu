@@ -1,0 +1,670 @@
+// moe_grouped_tc.cu — tensor-core (tcgen05 / TMEM / TMA) grouped expert GEMMs
+// for T > 1 tokens.
+//
+// "Decode throughput analysis report", code-level profiling section: the
+// prefill routed-expert path is the largest time-to-first-token cost and the
+// next step named there is a grouped GEMM over experts; "BI-V100 inference
+// work log", Part 7: once the tokens per expert grow, the MoE GEMM becomes a
+// real matrix product.  Swap-AB formulation per expert e with m_e tokens:
+//
+//   W13 pass   D[128 rows, N tokens] = [Wg rows i0..i0+63 ; Wu rows i0..i0+63] . Xs^T
+//              (K = H), epilogue act = silu(gate) * up for the 64 rows, stored as
+//              a two-term split act = hi + lo in the storage dtype (hi = rn(act),
+//              lo = rn(act - hi): 16 significant bits) so the next pass keeps
+//              fp32-level accuracy of the activation;
+//   W2 pass    D[128 rows (h), N tokens] = W2[e][h0..h0+127, :] . (hi + lo)^T
+//              (K = I, two MMAs per K step), epilogue y[pair, h] = weight(pair) * D.
+//
+// Both operands are K-major; tiles are moved by TMA (cp.async.bulk.tensor,
+// 128-byte swizzle) into a multi-stage shared-memory ring, multiplied by
+// tcgen05.mma (cta_group::1, kind::f16, fp32 accumulators in TMEM, double
+// buffered so the epilogue of one tile overlaps the MMAs of the next), and
+// read back with tcgen05.ld.  Warp roles: warp 0 issues TMA, warp 1 owns TMEM
+// and issues MMAs, warps 2-5 run the epilogue (one TMEM lane quarter each).
+// Every mbarrier wait is bounded by the GPU global timer; on expiry the kernel
+// records MOE_ERR_TIMEOUT, lets its own copies and MMAs finish (bounded),
+// frees its TMEM and returns.
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+constexpr int kTcThreads = 192;
+constexpr int kBK = 64;                 // K elements per stage: one 128-byte swizzle row
+constexpr uint32_t kTileA = 128 * 128;  // 128 rows x 128 bytes
+constexpr int kSmemBudget = 196 * 1024;
+
+struct TcTile {
+  int32_t e;     // expert id, E = shared expert
+  int32_t m;     // M-tile index within the expert
+  int32_t pos0;  // first sorted pair position of the N-tile
+  int32_t n;     // valid tokens in the tile
+};
+
+// ----------------------------------------------------------------- PTX
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+          smem_u32(dst)),
+      "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// 32 lanes x 16 consecutive fp32 columns of TMEM -> 16 registers per thread.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major tile written by TMA with the
+// 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart (SBO),
+// descriptor version 1, layout "128B swizzle".
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, A and B both DT
+// (fp16 = 0, bf16 = 1), both K-major, M = 128, N.
+template <int DT, int N>
+__device__ __forceinline__ constexpr uint32_t idesc_f16() {
+  constexpr uint32_t fmt = DT == MOE_BF16 ? 1u : 0u;
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(128 >> 4) << 24);
+}
+
+template <int DT>
+__device__ __forceinline__ void split_store(uint16_t* hi, uint16_t* lo, size_t off, float a) {
+  if constexpr (DT == MOE_BF16) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(a);
+    const __nv_bfloat16 l = __float2bfloat16_rn(a - __bfloat162float(h));
+    hi[off] = __bfloat16_as_ushort(h);
+    lo[off] = __bfloat16_as_ushort(l);
+  } else {
+    const __half h = __float2half_rn(a);
+    const __half l = __float2half_rn(a - __half2float(h));
+    hi[off] = __half_as_ushort(h);
+    lo[off] = __half_as_ushort(l);
+  }
+}
+
+// Bounded wait used by every role; false on timeout or when another role aborted.
+__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, uint64_t timeout, volatile int* abort) {
+  const uint64_t deadline = global_ns() + timeout;
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort || global_ns() > deadline) return false;
+  }
+  return true;
+}
+
+// OR of `v` over the 128 epilogue threads (named barrier 1 with reduction):
+// every epilogue thread gets the same answer, so they leave loops together
+// and none is left waiting at a named barrier.
+__device__ __forceinline__ bool epi_any(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, 1, 128, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v))
+      : "memory");
+  return r != 0;
+}
+
+// ======================================================= W13 + SiLU pass
+template <int DT, int N>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    tc_w13_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapAs,
+                  const __grid_constant__ CUtensorMap mapB, const TcTile* __restrict__ tiles,
+                  const int32_t* __restrict__ n_tiles_p, int H, int I, int Is, int E, int act_stride,
+                  uint16_t* __restrict__ act_hi, uint16_t* __restrict__ act_lo, Control* ctrl, uint64_t timeout) {
+  constexpr uint32_t kStage = kTileA + N * 128;
+  constexpr int kStages = (kSmemBudget - 128 * 17 * 4) / kStage > 8 ? 8 : (kSmemBudget - 128 * 17 * 4) / kStage;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* stg = reinterpret_cast<float*>(smem + kStages * kStage);  // [128][17] epilogue staging
+  __shared__ __align__(8) uint64_t full[kStages], empty[kStages], tfull[2], tempty[2], done;
+  __shared__ uint32_t tmem_base_s;
+  __shared__ volatile int s_abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], 4); }
+    mbar_init(&done, 1);
+    mbar_fence_init();
+    s_abort = 0;
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_s, 2 * N);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tmem_base_s;
+  const int ntiles = *n_tiles_p;
+  const int KB = H / kBK;
+
+  if (warp == 0) {
+    if (lane == 0) {  // ---------------------------------------------- TMA producer
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, issued_phase = 0;
+      for (int t = blockIdx.x; t < ntiles && !s_abort; t += gridDim.x) {
+        const TcTile tl = tiles[t];
+        const bool sh = tl.e == E;
+        const CUtensorMap* mA = sh ? &mapAs : &mapA;
+        const int ie = sh ? Is : I;
+        const int rowg = (sh ? 0 : tl.e * 2 * I) + tl.m * 64;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!tc_wait(&empty[stage], phase ^ 1u, timeout, &s_abort)) {
+            s_abort = 1;
+            report_error(ctrl, kDevTimeoutCopy, blockIdx.x);
+            break;
+          }
+          uint8_t* sA = smem + stage * kStage;
+          mbar_arrive_expect_tx(&full[stage], kStage);
+          tma_load_2d(sA, mA, &full[stage], kb * kBK, rowg);
+          tma_load_2d(sA + kTileA / 2, mA, &full[stage], kb * kBK, rowg + ie);
+          tma_load_2d(sA + kTileA, &mapB, &full[stage], kb * kBK, tl.pos0);
+          issued_mask |= 1u << stage;
+          issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // let every copy this thread issued land before the CTA exits
+      for (int s = 0; s < kStages; ++s)
+        if (issued_mask & (1u << s)) mbar_wait_until(&full[s], (issued_phase >> s) & 1u, global_ns() + timeout);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // ---------------------------------------------- MMA issuer
+      constexpr uint32_t idesc = idesc_f16<DT, N>();
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      for (int t = blockIdx.x; t < ntiles && !s_abort; t += gridDim.x, ++it) {
+        const int acc = it & 1;
+        if (!tc_wait(&tempty[acc], ((it >> 1) & 1) ^ 1u, timeout, &s_abort)) {
+          s_abort = 1;
+          report_error(ctrl, kDevTimeoutCopy, blockIdx.x);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tbase + static_cast<uint32_t>(acc * N);
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!tc_wait(&full[stage], phase, timeout, &s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sA = smem_u32(smem + stage * kStage);
+          const uint32_t sB = sA + kTileA;
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            tc_mma(d, sw128_desc(sA + 32 * k), sw128_desc(sB + 32 * k), idesc, (kb | k) != 0);
+          tc_commit(&empty[stage]);
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) {
+          s_abort = 1;
+          report_error(ctrl, kDevTimeoutCopy, blockIdx.x);
+          break;
+        }
+        tc_commit(&tfull[acc]);
+      }
+      tc_commit(&done);  // completes once every MMA issued above has completed
+      mbar_wait_until(&done, 0, global_ns() + timeout);
+    }
+  } else {  // ---------------------------------------------------- epilogue, 128 threads
+    const int q = warp & 3;
+    const int row = 32 * q + lane;
+    int it = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+      const TcTile tl = tiles[t];
+      const int acc = it & 1;
+      const bool ok = !s_abort && tc_wait(&tfull[acc], (it >> 1) & 1, timeout, &s_abort);
+      if (epi_any(!ok)) {
+        s_abort = 1;
+        report_error(ctrl, kDevTimeoutCopy, blockIdx.x);
+        break;
+      }
+      tc_fence_after();
+      for (int c0 = 0; c0 < tl.n; c0 += 16) {
+        float v[16];
+        tmem_ld16(tbase + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(acc * N + c0), v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) stg[row * 17 + j] = v[j];
+        named_bar_sync(1, 128);
+        if (row < 64) {
+          const int i = tl.m * 64 + row;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int col = c0 + j;
+            if (col < tl.n) {
+              const float g = stg[row * 17 + j], u = stg[(row + 64) * 17 + j];
+              split_store<DT>(act_hi, act_lo, static_cast<size_t>(tl.pos0 + col) * act_stride + i, silu_f(g) * u);
+            }
+          }
+        }
+        named_bar_sync(1, 128);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 2 * N);
+  }
+}
+
+// =========================================================== W2 pass
+template <int DT, int N>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    tc_w2_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapAs,
+                 const __grid_constant__ CUtensorMap mapHi, const __grid_constant__ CUtensorMap mapLo,
+                 const __grid_constant__ CUtensorMap mapHiS, const __grid_constant__ CUtensorMap mapLoS,
+                 const TcTile* __restrict__ tiles, const int32_t* __restrict__ n_tiles_p,
+                 const int32_t* __restrict__ perm, const float* __restrict__ topk_w,
+                 const float* __restrict__ gate_logits, int gate_stride, int has_gate, int T, int H, int I, int Is,
+                 int E, int k, float* __restrict__ y, Control* ctrl, uint64_t timeout) {
+  constexpr uint32_t kStage = kTileA + 2 * N * 128;
+  constexpr int kStages = kSmemBudget / kStage > 8 ? 8 : kSmemBudget / kStage;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t full[kStages], empty[kStages], tfull[2], tempty[2], done;
+  __shared__ uint32_t tmem_base_s;
+  __shared__ volatile int s_abort;
+  __shared__ int s_pair[N];
+  __shared__ float s_wt[N];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], 4); }
+    mbar_init(&done, 1);
+    mbar_fence_init();
+    s_abort = 0;
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_s, 2 * N);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tmem_base_s;
+  const int ntiles = *n_tiles_p;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, issued_phase = 0;
+      for (int t = blockIdx.x; t < ntiles && !s_abort; t += gridDim.x) {
+        const TcTile tl = tiles[t];
+        const bool sh = tl.e == E;
+        const CUtensorMap* mA = sh ? &mapAs : &mapA;
+        const CUtensorMap* mH = sh ? &mapHiS : &mapHi;
+        const CUtensorMap* mL = sh ? &mapLoS : &mapLo;
+        const int KB = (sh ? Is : I) / kBK;
+        const int rowa = (sh ? 0 : tl.e * H) + tl.m * 128;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!tc_wait(&empty[stage], phase ^ 1u, timeout, &s_abort)) {
+            s_abort = 1;
+            report_error(ctrl, kDevTimeoutCopy, blockIdx.x);
+            break;
+          }
+          uint8_t* sA = smem + stage * kStage;
+          mbar_arrive_expect_tx(&full[stage], kStage);
+          tma_load_2d(sA, mA, &full[stage], kb * kBK, rowa);
+          tma_load_2d(sA + kTileA, mH, &full[stage], kb * kBK, tl.pos0);
+          tma_load_2d(sA + kTileA + N * 128, mL, &full[stage], kb * kBK, tl.pos0);
+          issued_mask |= 1u << stage;
+          issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      for (int s = 0; s < kStages; ++s)
+        if (issued_mask & (1u << s)) mbar_wait_until(&full[s], (issued_phase >> s) & 1u, global_ns() + timeout);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16<DT, N>();
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      for (int t = blockIdx.x; t < ntiles && !s_abort; t += gridDim.x, ++it) {
+        const TcTile tl = tiles[t];
+        const int KB = (tl.e == E ? Is : I) / kBK;
+        const int acc = it & 1;
+        if (!tc_wait(&tempty[acc], ((it >> 1) & 1) ^ 1u, timeout, &s_abort)) {
+          s_abort = 1;
+          report_error(ctrl, kDevTimeoutCopy, blockIdx.x);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tbase + static_cast<uint32_t>(acc * N);
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!tc_wait(&full[stage], phase, timeout, &s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sA = smem_u32(smem + stage * kStage);
+          const uint32_t sH = sA + kTileA, sL = sH + N * 128;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            tc_mma(d, sw128_desc(sA + 32 * kk), sw128_desc(sH + 32 * kk), idesc, (kb | kk) != 0);
+            tc_mma(d, sw128_desc(sA + 32 * kk), sw128_desc(sL + 32 * kk), idesc, 1u);
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) {
+          s_abort = 1;
+          report_error(ctrl, kDevTimeoutCopy, blockIdx.x);
+          break;
+        }
+        tc_commit(&tfull[acc]);
+      }
+      tc_commit(&done);
+      mbar_wait_until(&done, 0, global_ns() + timeout);
+    }
+  } else {
+    const int q = warp & 3;
+    const int row = 32 * q + lane;
+    const int etid = threadIdx.x - 64;  // 0..127
+    int it = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+      const TcTile tl = tiles[t];
+      const int acc = it & 1;
+      if (epi_any(s_abort != 0)) break;  // also: previous tile's readers of s_pair / s_wt are done
+      for (int c = etid; c < tl.n; c += 128) {
+        const int p = perm[tl.pos0 + c];
+        s_pair[c] = p;
+        float wt;
+        if (p < T * k) wt = topk_w[p];
+        else wt = has_gate ? sigmoid_f(gate_logits[static_cast<size_t>(p - T * k) * gate_stride + E]) : 1.0f;
+        s_wt[c] = wt;
+      }
+      const bool ok = !s_abort && tc_wait(&tfull[acc], (it >> 1) & 1, timeout, &s_abort);
+      if (epi_any(!ok)) {  // the barrier also publishes s_pair / s_wt
+        s_abort = 1;
+        report_error(ctrl, kDevTimeoutCopy, blockIdx.x);
+        break;
+      }
+      tc_fence_after();
+      const int h = tl.m * 128 + row;
+      for (int c0 = 0; c0 < tl.n; c0 += 16) {
+        float v[16];
+        tmem_ld16(tbase + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(acc * N + c0), v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int col = c0 + j;
+          if (col < tl.n) y[static_cast<size_t>(s_pair[col]) * H + h] = s_wt[col] * v[j];
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 2 * N);
+  }
+}
+
+// ===================================================== schedule + gather
+// Tile lists of both passes from the per-expert counts/offsets (one CTA).
+// Layout of `sched`: [0] n13, [1] n2, then TcTile arrays at the offsets given.
+__global__ void __launch_bounds__(1024) tc_schedule_kernel(const int32_t* __restrict__ counts,
+                                                           const int32_t* __restrict__ offsets, int E, int I,
+                                                           int Is, int H, int N, int32_t* n13, int32_t* n2,
+                                                           TcTile* t13, TcTile* t2) {
+  __shared__ unsigned long long wtot[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n = E + 1;
+  // one expert per thread (n <= 1025: two per thread at most)
+  int a13[2] = {0, 0}, a2[2] = {0, 0}, cnt[2] = {0, 0};
+  for (int s = 0; s < 2; ++s) {
+    const int e = 2 * tid + s;
+    if (e < n) {
+      cnt[s] = counts[e];
+      const int ie = e == E ? Is : I;
+      const int nt = (cnt[s] + N - 1) / N;
+      a13[s] = ie > 0 ? nt * (ie / 64) : 0;
+      a2[s] = ie > 0 ? nt * (H / 128) : 0;
+    }
+  }
+  unsigned long long v = (static_cast<unsigned long long>(a13[0] + a13[1]) << 32) | static_cast<unsigned>(a2[0] + a2[1]);
+  unsigned long long incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long yv = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += yv;
+  }
+  if (lane == 31) wtot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    unsigned long long s = wtot[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long yv = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += yv;
+    }
+    wtot[lane] = s;
+  }
+  __syncthreads();
+  const unsigned long long before = incl - v + (warp ? wtot[warp - 1] : 0ull);
+  int b13 = static_cast<int>(before >> 32), b2 = static_cast<int>(before & 0xffffffffu);
+  for (int s = 0; s < 2; ++s) {
+    const int e = 2 * tid + s;
+    if (e >= n || cnt[s] == 0) {
+      b13 += a13[s];
+      b2 += a2[s];
+      continue;
+    }
+    const int ie = e == E ? Is : I;
+    const int nt = (cnt[s] + N - 1) / N;
+    const int m13 = ie / 64, m2 = H / 128;
+    for (int j = 0; j < nt; ++j) {
+      const int pos0 = offsets[e] + j * N;
+      const int nv = min(N, cnt[s] - j * N);
+      for (int mm = 0; mm < m13; ++mm) t13[b13 + j * m13 + mm] = TcTile{e, mm, pos0, nv};
+      for (int mm = 0; mm < m2; ++mm) t2[b2 + j * m2 + mm] = TcTile{e, mm, pos0, nv};
+    }
+    b13 += a13[s];
+    b2 += a2[s];
+  }
+  if (tid == 0) {
+    *n13 = static_cast<int>(wtot[31] >> 32);
+    *n2 = static_cast<int>(wtot[31] & 0xffffffffu);
+  }
+}
+
+// Xs[pos, :] = x[token of perm[pos], :] (16-byte chunks).
+__global__ void __launch_bounds__(256) tc_gather_kernel(const uint8_t* __restrict__ x, const int32_t* __restrict__ perm,
+                                                        int P, int T, int k, int H, uint8_t* __restrict__ xs) {
+  const int nch = H >> 3;
+  const size_t total = static_cast<size_t>(P) * nch;
+  for (size_t i = blockIdx.x * 256ull + threadIdx.x; i < total; i += static_cast<size_t>(gridDim.x) * 256) {
+    const int pos = static_cast<int>(i / nch), c = static_cast<int>(i - static_cast<size_t>(pos) * nch);
+    const int p = perm[pos];
+    const int t = p < T * k ? p / k : p - T * k;
+    const uint4 v = ld_nc16(x + (static_cast<size_t>(t) * H + 8 * c) * 2);
+    *reinterpret_cast<uint4*>(xs + (static_cast<size_t>(pos) * H + 8 * c) * 2) = v;
+  }
+}
+
+// ================================================================ host
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D K-major map: `inner` elements per row (contiguous), `outer` rows of
+// `row_stride` bytes; box of 64 x box_rows, 128-byte swizzle.
+static bool make_map(CUtensorMap* m, int dtype, const void* base, uint64_t inner, uint64_t outer,
+                     uint64_t row_stride, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_stride};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(m, dtype == MOE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                        const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool tc_shape_ok(const moe_cfg_t& c) {
+  return c.dtype == MOE_BF16 && c.hidden % 128 == 0 && c.inter % 64 == 0 && c.shared_inter % 64 == 0;
+}
+
+bool tc_path_supported(const moe_cfg_t& c) { return tc_shape_ok(c) && encode_fn() != nullptr; }
+
+template <int N>
+static size_t tc_smem13() {
+  constexpr uint32_t st = kTileA + N * 128;
+  constexpr int ns = (kSmemBudget - 128 * 17 * 4) / st > 8 ? 8 : (kSmemBudget - 128 * 17 * 4) / st;
+  return static_cast<size_t>(ns) * st + 128 * 17 * 4 + 1024;
+}
+template <int N>
+static size_t tc_smem2() {
+  constexpr uint32_t st = kTileA + 2 * N * 128;
+  constexpr int ns = kSmemBudget / st > 8 ? 8 : kSmemBudget / st;
+  return static_cast<size_t>(ns) * st + 1024;
+}
+
+template <int N>
+static moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws, const WsLayout& L,
+                                     int32_t T, cudaStream_t st) {
+  constexpr int DT = MOE_BF16;
+  const int H = c.hidden, E = c.n_experts, k = c.top_k, I = c.inter, Is = c.shared_inter;
+  const int Imax = I > Is ? I : Is;
+  const int P = static_cast<int>(L.pairs);
+  Control* ctrl = reinterpret_cast<Control*>(ws + L.ctrl);
+  int32_t* counts = reinterpret_cast<int32_t*>(ws + L.g_counts);
+  int32_t* offsets = reinterpret_cast<int32_t*>(ws + L.g_offsets);
+  int32_t* perm = reinterpret_cast<int32_t*>(ws + L.g_perm);
+  int32_t* sched = reinterpret_cast<int32_t*>(ws + L.tc_sched);
+  TcTile* t13 = reinterpret_cast<TcTile*>(ws + L.tc_tiles13);
+  TcTile* t2 = reinterpret_cast<TcTile*>(ws + L.tc_tiles2);
+  uint8_t* xs = ws + L.tc_xs;
+  uint16_t* ahi = reinterpret_cast<uint16_t*>(ws + L.tc_act_hi);
+  uint16_t* alo = reinterpret_cast<uint16_t*>(ws + L.tc_act_lo);
+  float* y = reinterpret_cast<float*>(ws + L.g_y);
+  const float* glog = reinterpret_cast<const float*>(ws + L.r_logits);
+  const int gate_stride = c.has_shared_gate ? E + 1 : E;
+  const uint64_t timeout = wait_timeout_ns();
+
+  tc_schedule_kernel<<<1, 1024, 0, st>>>(counts, offsets, E, I, Is, H, N, sched, sched + 1, t13, t2);
+  if (moe_status_t s = check_launch("tc_schedule_kernel")) return s;
+  const int sms = sm_count();
+  const size_t gchunks = static_cast<size_t>(P) * (H / 8);
+  const int gg = static_cast<int>((gchunks + 255) / 256 < static_cast<size_t>(sms) * 8 ? (gchunks + 255) / 256
+                                                                                      : static_cast<size_t>(sms) * 8);
+  tc_gather_kernel<<<gg, 256, 0, st>>>(static_cast<const uint8_t*>(p.x), perm, P, T, k, H, xs);
+  if (moe_status_t s = check_launch("tc_gather_kernel")) return s;
+
+  CUtensorMap mA, mAs, mB, mW2, mW2s, mHi, mLo, mHiS, mLoS;
+  const void* sw13 = p.shared_w13 ? p.shared_w13 : p.w13;
+  const void* sw2 = p.shared_w2 ? p.shared_w2 : p.w2;
+  const int IsM = Is > 0 ? Is : I;
+  bool ok = make_map(&mA, DT, p.w13, H, static_cast<uint64_t>(E) * 2 * I, static_cast<uint64_t>(H) * 2, 64) &&
+            make_map(&mAs, DT, sw13, H, 2ull * IsM, static_cast<uint64_t>(H) * 2, 64) &&
+            make_map(&mB, DT, xs, H, P, static_cast<uint64_t>(H) * 2, N) &&
+            make_map(&mW2, DT, p.w2, I, static_cast<uint64_t>(E) * H, static_cast<uint64_t>(I) * 2, 128) &&
+            make_map(&mW2s, DT, sw2, IsM, H, static_cast<uint64_t>(IsM) * 2, 128) &&
+            make_map(&mHi, DT, ahi, I, P, static_cast<uint64_t>(Imax) * 2, N) &&
+            make_map(&mLo, DT, alo, I, P, static_cast<uint64_t>(Imax) * 2, N) &&
+            make_map(&mHiS, DT, ahi, IsM, P, static_cast<uint64_t>(Imax) * 2, N) &&
+            make_map(&mLoS, DT, alo, IsM, P, static_cast<uint64_t>(Imax) * 2, N);
+  if (!ok) return set_error(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+
+  const size_t s13 = tc_smem13<N>(), s2 = tc_smem2<N>();
+  cudaFuncSetAttribute(tc_w13_kernel<DT, N>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s13));
+  cudaFuncSetAttribute(tc_w2_kernel<DT, N>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s2));
+  const int g13 = static_cast<int>(L.tc_max13 < sms ? L.tc_max13 : sms);
+  const int g2 = static_cast<int>(L.tc_max2 < sms ? L.tc_max2 : sms);
+  tc_w13_kernel<DT, N><<<g13 > 0 ? g13 : 1, kTcThreads, s13, st>>>(mA, mAs, mB, t13, sched, H, I, Is, E, Imax, ahi,
+                                                                   alo, ctrl, timeout);
+  if (moe_status_t s = check_launch("tc_w13_kernel")) return s;
+  tc_w2_kernel<DT, N><<<g2 > 0 ? g2 : 1, kTcThreads, s2, st>>>(mW2, mW2s, mHi, mLo, mHiS, mLoS, t2, sched + 1, perm,
+                                                               p.topk_w, glog, gate_stride, c.has_shared_gate, T, H,
+                                                               I, Is, E, k, y, ctrl, timeout);
+  if (moe_status_t s = check_launch("tc_w2_kernel")) return s;
+  stat_kernels(4);
+  return MOE_OK;
+}
+
+int tc_tile_n(const moe_cfg_t& c, int32_t T) {
+  const double avg = static_cast<double>(T) * c.top_k / c.n_experts;
+  return avg > 48.0 ? 128 : 64;
+}
+
+moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws, const WsLayout& L, int32_t T,
+                              cudaStream_t st) {
+  if (L.tc_n == 128) return launch_tc_passes<128>(c, p, ws, L, T, st);
+  return launch_tc_passes<64>(c, p, ws, L, T, st);
+}
+
+}  // namespace moe

@@ -28,6 +28,16 @@ struct WsLayout {
   size_t g_tiles = 0;     // [max_tiles + 1] int32 x2: (expert, first row) per tile
   size_t g_act = 0;       // [P, max(I, Is)] fp32
   size_t g_y = 0;         // [P, H] fp32 weighted expert outputs
+  // tensor-core grouped path (T > 1, bf16, H % 128 == 0, I and Is % 64 == 0)
+  size_t tc_sched = 0;    // 2 int32: tile counts of the two passes
+  size_t tc_tiles13 = 0;  // [tc_max13] tiles of the W13 pass
+  size_t tc_tiles2 = 0;   // [tc_max2] tiles of the W2 pass
+  size_t tc_xs = 0;       // [P, H] x rows gathered in expert order
+  size_t tc_act_hi = 0;   // [P, max(I, Is)] activation, leading term
+  size_t tc_act_lo = 0;   // [P, max(I, Is)] activation, remainder term
+  int tc_n = 0;           // tokens per tile (0 = path not laid out)
+  int64_t tc_max13 = 0;
+  int64_t tc_max2 = 0;
   size_t total = 0;
   int64_t pairs = 0;      // P = T*k + (Is ? T : 0)
   int64_t max_tiles = 0;
@@ -43,6 +53,7 @@ moe_status_t check_launch(const char* what);
 void stat_decode();
 void stat_router();
 void stat_grouped();
+void stat_grouped_tc();
 void stat_kernels(uint64_t n);
 
 // Device properties cached per device.
@@ -72,6 +83,13 @@ moe_status_t launch_router(const moe_cfg_t& c, const void* x, const void* router
 moe_status_t launch_grouped(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws, const WsLayout& L,
                             int32_t T, cudaStream_t st);
 moe_status_t launch_wait_test(uint8_t* ws, cudaStream_t st);
+
+// Tensor-core grouped passes (moe_grouped_tc.cu).
+bool tc_shape_ok(const moe_cfg_t& c);        // shape/dtype eligibility (host only)
+bool tc_path_supported(const moe_cfg_t& c);  // eligibility and the TMA encoder is available
+int tc_tile_n(const moe_cfg_t& c, int32_t T);
+moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws, const WsLayout& L, int32_t T,
+                              cudaStream_t st);
 
 // Grid size of the single-launch decode kernel for cfg c.
 int decode_grid(const moe_cfg_t& c);

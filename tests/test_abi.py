@@ -60,7 +60,7 @@ def _topk(m):
 
 @pytest.mark.parametrize("field,value,code", [
     ("hidden", 0, 1), ("inter", 12, 2), ("top_k", 33, 2), ("top_k", 0, 1), ("dtype", 3, 2),
-    ("n_experts", 2000, 2), ("flags", 1, 1), ("norm_topk", 2, 1),
+    ("n_experts", 2000, 2), ("flags", 4, 1), ("flags", 3, 1), ("norm_topk", 2, 1),
 ])
 def test_bad_cfg_is_rejected_on_host(m, field, value, code):
     c = m.MoeCfg(256, 16, 2, 64, 0, m.MOE_F16).c()
@@ -140,7 +140,8 @@ def test_timeout_setting(m):
 def test_stats_roundtrip(m):
     m.moe_reset_stats()
     s = m.moe_get_stats()
-    assert s == {"decode_fused_calls": 0, "router_calls": 0, "grouped_calls": 0, "kernels_launched": 0}
+    assert s == {"decode_fused_calls": 0, "router_calls": 0, "grouped_calls": 0, "grouped_tc_calls": 0,
+                 "kernels_launched": 0}
 
 
 def test_python_binding_checks_shapes(m):
@@ -149,3 +150,13 @@ def test_python_binding_checks_shapes(m):
     with pytest.raises(ValueError):
         m.moe_router_topk(cfg, x, torch.zeros(16, 256, dtype=torch.float16), torch.zeros(1, 2, dtype=torch.int32),
                           torch.zeros(1, 2), torch.zeros(16, dtype=torch.uint8))
+
+
+def test_tensor_core_path_workspace_is_laid_out_for_bf16_shapes(m):
+    bf = m.MoeCfg(2048, 256, 8, 512, 512, m.MOE_BF16, has_shared_gate=1)
+    fp = m.MoeCfg(2048, 256, 8, 512, 512, m.MOE_F16, has_shared_gate=1)
+    T = 512
+    P = T * 8 + T
+    extra = m.moe_workspace_bytes(bf, T) - m.moe_workspace_bytes(fp, T)
+    # gathered x rows plus the two activation terms
+    assert extra >= P * 2048 * 2 + 2 * P * 512 * 2

@@ -1,0 +1,57 @@
+"""Host logic of bench.py: the bytes model, and the multi-rank aggregation
+(barrier, max over ranks) on two gloo ranks on the CPU."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+import moe_synth
+
+
+def test_algorithmic_bytes_per_layer():
+    assert bench.algorithmic_bytes(moe_synth.workload("sharded_decode")) == 15_212_544
+    assert bench.algorithmic_bytes(moe_synth.workload("full_decode")) == 57_683_968
+
+
+def test_layer_bytes_match_generated_tensors():
+    wl = moe_synth.workload("tiny")
+    d = moe_synth.make_layer(wl, 0, 1)
+    n = sum(v.numel() * v.element_size() for k, v in d.items() if v is not None and k != "x")
+    assert n == wl.layer_bytes()
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    ws, r, local = bench.dist_setup()
+    assert ws == world and r == rank
+    bench.barrier(ws)
+    m = bench.reduce_max(float(10 * (rank + 1)), ws)
+    q.put((rank, m))
+    dist.destroy_process_group()
+
+
+def test_two_rank_max_over_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    res = sorted(q.get(timeout=5) for _ in range(2))
+    assert res == [(0, 20.0), (1, 20.0)]

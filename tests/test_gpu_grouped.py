@@ -20,8 +20,8 @@ def m():
     return mod
 
 
-def _grouped(m, wl, g, T, out_dtype=None, ws=None):
-    cfg = m.cfg_from_workload(wl, out_dtype)
+def _grouped(m, wl, g, T, out_dtype=None, ws=None, flags=0):
+    cfg = m.cfg_from_workload(wl, out_dtype, flags)
     ids = torch.full((T, wl.top_k), -1, dtype=torch.int32, device=DEV)
     w = torch.full((T, wl.top_k), float("nan"), dtype=torch.float32, device=DEV)
     out = torch.full((T, wl.hidden), float("nan"), dtype=cfg.out_torch_dtype, device=DEV)
@@ -44,24 +44,30 @@ def _check_tokens(ids, w, out, ref, tokens, k):
     assert ok >= max(1, int(0.8 * len(tokens)))
 
 
+SIMT, TC = 1, 2
+
+
+@pytest.mark.parametrize("flags", [SIMT, TC], ids=["simt", "tc"])
 @pytest.mark.parametrize("T", [2, 4, 8, 16, 64])
-def test_small_batch_zipf(m, T):
+def test_small_batch_zipf(m, T, flags):
     wl = moe_synth.workload("small_batch")
     g = moe_synth.make_layer(wl, 0, T, device=DEV)
     m.moe_reset_stats()
-    ids, w, out = _grouped(m, wl, g, T)
-    assert m.moe_get_stats()["grouped_calls"] == 1
+    ids, w, out = _grouped(m, wl, g, T, flags=flags)
+    st = m.moe_get_stats()
+    assert st["grouped_calls"] == 1 and st["grouped_tc_calls"] == (1 if flags == TC else 0)
     tokens = list(range(T)) if T <= 8 else sorted(np.random.default_rng(T).choice(T, 8, replace=False).tolist())
     ref = oracle_sampled(wl, g, tokens)
     _check_tokens(ids, w, out, ref, tokens, wl.top_k)
 
 
+@pytest.mark.parametrize("flags", [SIMT, TC], ids=["simt", "tc"])
 @pytest.mark.parametrize("T", [3, 65, 130])
-def test_odd_token_counts_small_shapes(m, T):
-    wl = moe_synth.Workload("odd", 256, 32, 4, 64, 32, moe_synth.BF16, 1, 1.0, 0.05, 0.05, preset_id=6)
+def test_odd_token_counts_small_shapes(m, T, flags):
+    wl = moe_synth.Workload("odd", 256, 32, 4, 64, 64, moe_synth.BF16, 1, 1.0, 0.05, 0.05, preset_id=6)
     d = moe_synth.make_layer(wl, 0, T)
     g = {k: (v.to(DEV) if v is not None else None) for k, v in d.items()}
-    ids, w, out = _grouped(m, wl, g, T, out_dtype=3)
+    ids, w, out = _grouped(m, wl, g, T, out_dtype=3, flags=flags)
     ref = oracle_full(wl, d)
     gaps = min_rank_gap(ref["logits"], wl.top_k)
     good = gaps > 1e-5
@@ -69,16 +75,25 @@ def test_odd_token_counts_small_shapes(m, T):
     parity(out, ref["out"])
 
 
-def test_token_permutation_permutes_output(m):
+@pytest.mark.parametrize("flags", [SIMT, TC], ids=["simt", "tc"])
+def test_token_permutation_permutes_output(m, flags):
     wl = moe_synth.workload("small_batch")
     T = 16
     g = moe_synth.make_layer(wl, 1, T, device=DEV)
-    _, _, out = _grouped(m, wl, g, T)
+    _, _, out = _grouped(m, wl, g, T, flags=flags)
     perm = torch.randperm(T, generator=torch.Generator().manual_seed(0)).to(DEV)
     g2 = dict(g)
     g2["x"] = g["x"][perm].contiguous()
-    _, _, out2 = _grouped(m, wl, g2, T)
+    _, _, out2 = _grouped(m, wl, g2, T, flags=flags)
     assert torch.equal(out2, out[perm])
+
+
+def test_tc_path_rejects_fp16(m):
+    wl = moe_synth.workload("sharded_decode")
+    g = moe_synth.make_layer(wl, 0, 4, device=DEV)
+    with pytest.raises(m.MoeError) as ei:
+        _grouped(m, wl, g, 4, flags=TC)
+    assert ei.value.code == 2
 
 
 def test_grouped_t1_dispatches_to_decode_kernel(m):
@@ -92,11 +107,32 @@ def test_grouped_t1_dispatches_to_decode_kernel(m):
     _check_tokens(ids, w, out, ref, [0], wl.top_k)
 
 
-def test_chunked_prefill_512(m):
+@pytest.mark.parametrize("flags", [SIMT, TC], ids=["simt", "tc"])
+def test_chunked_prefill_512(m, flags):
     wl = moe_synth.workload("chunked_prefill")
     T = 512
     g = moe_synth.make_layer(wl, 0, T, device=DEV)
-    ids, w, out = _grouped(m, wl, g, T)
+    ids, w, out = _grouped(m, wl, g, T, flags=flags)
     tokens = [0, 1, 255, 256, 511] + sorted(np.random.default_rng(5).choice(T, 3, replace=False).tolist())
     ref = oracle_sampled(wl, g, tokens)
     _check_tokens(ids, w, out, ref, tokens, wl.top_k)
+
+
+def test_chunked_prefill_4096_tc(m):
+    wl = moe_synth.workload("chunked_prefill")
+    T = 4096
+    g = moe_synth.make_layer(wl, 0, T, device=DEV)
+    ids, w, out = _grouped(m, wl, g, T, flags=TC)
+    tokens = [0, 4095] + sorted(np.random.default_rng(9).choice(T, 4, replace=False).tolist())
+    ref = oracle_sampled(wl, g, tokens)
+    _check_tokens(ids, w, out, ref, tokens, wl.top_k)
+
+
+def test_simt_and_tc_paths_agree(m):
+    wl = moe_synth.workload("chunked_prefill")
+    T = 300
+    g = moe_synth.make_layer(wl, 1, T, device=DEV)
+    i1, w1, o1 = _grouped(m, wl, g, T, out_dtype=3, flags=SIMT)
+    i2, w2, o2 = _grouped(m, wl, g, T, out_dtype=3, flags=TC)
+    assert torch.equal(i1, i2) and torch.equal(w1, w2)
+    parity(o2, o1.double().cpu().numpy(), max_err_frac=1e-3, rel_l1=1e-4)
