@@ -47,7 +47,7 @@ def _check_tokens(ids, w, out, ref, tokens, k):
 SIMT, TC = 1, 2
 
 
-@pytest.mark.parametrize("flags", [SIMT, TC], ids=["simt", "tc"])
+@pytest.mark.parametrize("flags", [SIMT, TC], ids=["simt", "tcgen05"])
 @pytest.mark.parametrize("T", [2, 4, 8, 16, 64])
 def test_small_batch_zipf(m, T, flags):
     wl = moe_synth.workload("small_batch")
@@ -61,7 +61,7 @@ def test_small_batch_zipf(m, T, flags):
     _check_tokens(ids, w, out, ref, tokens, wl.top_k)
 
 
-@pytest.mark.parametrize("flags", [SIMT, TC], ids=["simt", "tc"])
+@pytest.mark.parametrize("flags", [SIMT, TC], ids=["simt", "tcgen05"])
 @pytest.mark.parametrize("T", [3, 65, 130])
 def test_odd_token_counts_small_shapes(m, T, flags):
     wl = moe_synth.Workload("odd", 256, 32, 4, 64, 64, moe_synth.BF16, 1, 1.0, 0.05, 0.05, preset_id=6)
@@ -75,7 +75,7 @@ def test_odd_token_counts_small_shapes(m, T, flags):
     parity(out, ref["out"])
 
 
-@pytest.mark.parametrize("flags", [SIMT, TC], ids=["simt", "tc"])
+@pytest.mark.parametrize("flags", [SIMT, TC], ids=["simt", "tcgen05"])
 def test_token_permutation_permutes_output(m, flags):
     wl = moe_synth.workload("small_batch")
     T = 16
@@ -88,7 +88,7 @@ def test_token_permutation_permutes_output(m, flags):
     assert torch.equal(out2, out[perm])
 
 
-def test_tc_path_rejects_fp16(m):
+def test_tcgen05_path_rejects_fp16(m):
     wl = moe_synth.workload("sharded_decode")
     g = moe_synth.make_layer(wl, 0, 4, device=DEV)
     with pytest.raises(m.MoeError) as ei:
@@ -107,7 +107,7 @@ def test_grouped_t1_dispatches_to_decode_kernel(m):
     _check_tokens(ids, w, out, ref, [0], wl.top_k)
 
 
-@pytest.mark.parametrize("flags", [SIMT, TC], ids=["simt", "tc"])
+@pytest.mark.parametrize("flags", [SIMT, TC], ids=["simt", "tcgen05"])
 def test_chunked_prefill_512(m, flags):
     wl = moe_synth.workload("chunked_prefill")
     T = 512
@@ -118,7 +118,7 @@ def test_chunked_prefill_512(m, flags):
     _check_tokens(ids, w, out, ref, tokens, wl.top_k)
 
 
-def test_chunked_prefill_4096_tc(m):
+def test_chunked_prefill_4096_tcgen05(m):
     wl = moe_synth.workload("chunked_prefill")
     T = 4096
     g = moe_synth.make_layer(wl, 0, T, device=DEV)
@@ -128,7 +128,7 @@ def test_chunked_prefill_4096_tc(m):
     _check_tokens(ids, w, out, ref, tokens, wl.top_k)
 
 
-def test_simt_and_tc_paths_agree(m):
+def test_simt_and_tcgen05_paths_agree(m):
     wl = moe_synth.workload("chunked_prefill")
     T = 300
     g = moe_synth.make_layer(wl, 1, T, device=DEV)
