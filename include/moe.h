@@ -170,6 +170,32 @@ MOE_API moe_status_t moe_grouped_forward(const moe_cfg_t* cfg, const void* x, co
                                  const void* shared_w2, const void* shared_gate_w, moe_topk_t topk,
                                  void* out, void* ws, size_t ws_bytes, int32_t T, void* stream);
 
+/* Allocation-free variant of moe_decode_forward (T = 1).  The pages have no
+ * counterpart; this entry exists for callers that cannot allocate device
+ * memory and so cannot hand over the workspace moe_decode_forward needs:
+ * code running inside a fixed device-memory pool reserved at start-up, where a
+ * new cudaMalloc fails or is not allowed, or a plugin that only receives input
+ * and output pointers from its host framework.  The scratch (the control block
+ * and the words the CTAs exchange) lives in one fixed device array inside the
+ * library, MOE_NOALLOC_SCRATCH_BYTES long, which every GPU that loads the
+ * library keeps until the process exits.  A cfg whose workspace
+ * (moe_workspace_bytes(cfg, 1)) is larger is rejected with
+ * MOE_ERR_UNSUPPORTED.  The first call on each device looks up the array's
+ * device address (cudaGetSymbolAddress) with that device current; make that
+ * first call before any stream capture.  Each call zero-fills the part of the
+ * array it uses on `stream`, then enqueues the same kernel as
+ * moe_decode_forward; it allocates nothing.  All calls share the one array, so
+ * calls that can overlap on the GPU (other streams, other host threads) race
+ * and must be serialised by the caller.  The device status word is in that
+ * array too: moe_query_status cannot read it; host-side errors are returned
+ * as for every other call.  Arguments as moe_decode_forward, minus the
+ * workspace. */
+#define MOE_NOALLOC_SCRATCH_BYTES (256u * 1024u)
+MOE_API moe_status_t moe_decode_forward_noalloc(const moe_cfg_t* cfg, const void* x, const void* router_w,
+                                                const void* w13, const void* w2, const void* shared_w13,
+                                                const void* shared_w2, const void* shared_gate_w,
+                                                moe_topk_t topk, void* out, void* stream);
+
 /* Synchronise `stream`, then read and clear the device status word of `ws`.
  * Returns MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE (or MOE_ERR_CUDA if the
  * synchronisation failed); moe_last_error() then names the check that fired. */

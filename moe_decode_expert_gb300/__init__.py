@@ -31,7 +31,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 # Every symbol include/moe.h declares.
 EXPORTS = ("moe_abi_version", "moe_workspace_bytes", "moe_workspace_init", "moe_router_topk",
            "moe_decode_forward", "moe_grouped_forward", "moe_query_status", "moe_last_error",
-           "moe_get_stats", "moe_reset_stats", "moe_set_wait_timeout_ns", "moe_test_wait_timeout")
+           "moe_get_stats", "moe_reset_stats", "moe_set_wait_timeout_ns", "moe_test_wait_timeout",
+           "moe_decode_forward_noalloc")
 
 
 class MoeError(RuntimeError):
@@ -112,6 +113,7 @@ def _load():
         "moe_reset_stats": ([], None),
         "moe_set_wait_timeout_ns": ([u64], ctypes.c_int),
         "moe_test_wait_timeout": ([vp, sz, vp], ctypes.c_int),
+        "moe_decode_forward_noalloc": ([cfgp, vp, vp, vp, vp, vp, vp, vp, moe_topk_t, vp, vp], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -248,6 +250,15 @@ def moe_decode_forward(cfg: MoeCfg, x, router_w, w13, w2, shared_w13, shared_w2,
     args = _block_args(cfg, x, router_w, w13, w2, shared_w13, shared_w2, shared_gate_w, ids, weights, out, 1)
     c = cfg.c()
     _check(_load().moe_decode_forward(ctypes.byref(c), *args, _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_decode_forward_noalloc(cfg: MoeCfg, x, router_w, w13, w2, shared_w13, shared_w2, shared_gate_w, ids,
+                               weights, out, stream=None):
+    """moe_decode_forward for callers that cannot allocate a workspace: the
+    scratch is a fixed array inside the library (see include/moe.h)."""
+    args = _block_args(cfg, x, router_w, w13, w2, shared_w13, shared_w2, shared_gate_w, ids, weights, out, 1)
+    c = cfg.c()
+    _check(_load().moe_decode_forward_noalloc(ctypes.byref(c), *args, _stream(stream)))
 
 
 def moe_grouped_forward(cfg: MoeCfg, x, router_w, w13, w2, shared_w13, shared_w2, shared_gate_w, ids, weights,
