@@ -46,6 +46,30 @@ def algorithmic_bytes(wl, T=1) -> int:
     return 2 * n + 2 * T * H * 2
 
 
+def kernel_source_hash() -> str:
+    """Hash of the sources the single-launch decode kernel is built from."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("moe_decode.cu", "moe_common.cuh"):
+        with open(os.path.join(ROOT, "moe_decode_expert_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(wl):
+    """DRAM bytes per launch from the committed ncu summary of this kernel and
+    workload, or None when there is none or the kernel changed since."""
+    p = os.path.join(ROOT, "profiles", f"decode_fused_kernel_{wl.name}.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        pj = json.load(f)
+    if pj.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    per_layer = pj.get("dram_bytes_per_launch")
+    return per_layer
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -291,12 +315,7 @@ def run_ours(args, wl, ws_n, rank, local):
     alg = algorithmic_bytes(wl)
     peak, peak_kind = measured_peaks()
     achieved = alg / (us_layer * 1e-6) / 1e9
-    prof = os.path.join(ROOT, "profiles", f"decode_fused_kernel_{wl.name}.json")
-    traffic = None
-    if os.path.exists(prof):
-        with open(prof) as f:
-            pj = json.load(f)
-        traffic = pj.get("dram_bytes_per_launch")
+    traffic = profiled_traffic(wl)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws_n, "steps": K, "warmup": W,
         "ms_per_step": ms_max / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
