@@ -210,7 +210,7 @@ def run_reference(args, wl, ws_, rank):
 def config_of(wl):
     return {"workload": f"{wl.name}: H={wl.hidden} E={wl.n_experts} top-{wl.top_k} I={wl.inter} "
                         f"shared I={wl.shared_inter}{' +sigmoid gate' if wl.has_shared_gate else ''} "
-                        f"{'fp16' if wl.dtype == 1 else 'bf16'} T=1, {wl.layers} layers rotated",
+                        f"{'fp16' if wl.dtype == 1 else 'bf16'} T={wl.T}, {wl.layers} layers rotated",
             "T": 1, "layers": wl.layers, "global_batch": 1, "seq_len": 1,
             "parallelism": "replicas",
             "l2": f"inputs larger than L2: {wl.layers} layers x {wl.layer_bytes() / 1e6:.0f} MB of weights, "
@@ -279,21 +279,33 @@ def run_ours(args, wl, ws_n, rank, local):
     m.moe_query_status(ws, stream)
 
     # ------------------------------------------------ end to end, host buffers
-    E2E_STEPS = max(5, min(200, K // 20))
+    # The 36 public-API calls of a step captured once in a CUDA graph (as a
+    # decode server would); each step copies its inputs from pinned host memory,
+    # replays the graph and copies the outputs back, then synchronises.
+    E2E_STEPS = max(20, min(1000, K // 3))
     xh = torch.empty(L, 1, H, dtype=cfg.torch_dtype, pin_memory=True)
     xh.copy_(torch.stack([xs[0][l] for l in range(L)]).cpu())
     xd = torch.empty(L, 1, H, dtype=cfg.torch_dtype, device=dev)
     oh = torch.empty(L, 1, H, dtype=cfg.out_torch_dtype, pin_memory=True)
+    ge = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(ge, stream=stream):
+        for l in range(L):
+            g = layers[l]
+            m.moe_decode_forward(cfg, xd[l], g["router_w"], g["w13"], g["w2"], g["shared_w13"],
+                                 g["shared_w2"], g["shared_gate_w"], ids[l], wts[l], outs[l], ws, stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            xd.copy_(xh, non_blocking=True)
+            ge.replay()
+            oh.copy_(outs, non_blocking=True)
+        stream.synchronize()
     torch.cuda.synchronize()
     barrier(ws_n)
     t0 = time.perf_counter()
     with torch.cuda.stream(stream):
         for _ in range(E2E_STEPS):
             xd.copy_(xh, non_blocking=True)
-            for l in range(L):
-                g = layers[l]
-                m.moe_decode_forward(cfg, xd[l], g["router_w"], g["w13"], g["w2"], g["shared_w13"],
-                                     g["shared_w2"], g["shared_gate_w"], ids[l], wts[l], outs[l], ws, stream)
+            ge.replay()
             oh.copy_(outs, non_blocking=True)
             stream.synchronize()
     e2e_s = reduce_max(time.perf_counter() - t0, ws_n)
@@ -331,11 +343,114 @@ def run_ours(args, wl, ws_n, rank, local):
         "cpu_baseline": cpu,
         "e2e": {"value": E2E_STEPS * ws_n / e2e_s, "unit": "tokens/s",
                 "h2d_bytes_per_step": L * H * 2, "d2h_bytes_per_step": L * H * outs.element_size(),
-                "path": "moe_decode_forward per layer through the C ABI (no graph), pinned host x in, out back"},
+                "path": "36 moe_decode_forward calls captured once in a CUDA graph; per step: pinned H2D of x, "
+                        "graph replay, D2H of out, stream synchronise"},
         "gpu_launches": K * L,
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)
+
+
+def grouped_bytes(wl, T, n_distinct):
+    """Algorithmic bytes of one T-token grouped layer: router, each distinct
+    selected expert's W13 and W2 once, the shared expert (+gate), x and out."""
+    H, E, I, Is = wl.hidden, wl.n_experts, wl.inter, wl.shared_inter
+    n = E * H + n_distinct * 3 * I * H + 3 * Is * H + (H if wl.has_shared_gate else 0)
+    return 2 * n + 2 * 2 * T * H
+
+
+def grouped_flops(wl, T):
+    H, E, k, I, Is = wl.hidden, wl.n_experts, wl.top_k, wl.inter, wl.shared_inter
+    return 2 * T * (E * H + k * 3 * I * H + 3 * Is * H)
+
+
+def run_grouped(args, wl, ws_n, rank, local):
+    """T > 1 workloads (small-batch decode, chunked prefill): one step = one
+    grouped forward of T tokens through every layer, captured in a CUDA graph."""
+    import moe_decode_expert_gb300 as m
+
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    T = args.T or wl.T
+    cfg = m.cfg_from_workload(wl)
+    L = wl.layers
+    H, k = wl.hidden, wl.top_k
+    layers = [moe_synth.make_layer(wl, l, T, device=dev) for l in range(L)]
+    outs = torch.empty(L, T, H, dtype=cfg.out_torch_dtype, device=dev)
+    ids = torch.empty(L, T, k, dtype=torch.int32, device=dev)
+    wts = torch.empty(L, T, k, dtype=torch.float32, device=dev)
+    ws = m.alloc_workspace(cfg, T, dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step():
+        for l in range(L):
+            g = layers[l]
+            m.moe_grouped_forward(cfg, g["x"], g["router_w"], g["w13"], g["w2"], g["shared_w13"],
+                                  g["shared_w2"], g["shared_gate_w"], ids[l], wts[l], outs[l], ws, stream)
+
+    m.moe_reset_stats()
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    m.moe_query_status(ws, stream)
+    st = m.moe_get_stats()
+    kernels_per_layer = st["kernels_launched"] // L
+    path = "tcgen05" if st["grouped_tc_calls"] else "cuda-core"
+    gph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gph, stream=stream):
+        step()
+    K, W = args.steps, args.warmup
+    with torch.cuda.stream(stream):
+        for _ in range(W):
+            gph.replay()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(ws_n)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(K):
+            gph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms_max = reduce_max(e0.elapsed_time(e1), ws_n)
+    m.moe_query_status(ws, stream)
+    if rank != 0:
+        return
+    distinct = [int(torch.unique(ids[l]).numel()) for l in range(L)]
+    alg = sum(grouped_bytes(wl, T, u) for u in distinct) / L
+    us_layer = ms_max * 1e3 / (K * L)
+    peak, peak_kind = measured_peaks()
+    achieved = alg / (us_layer * 1e-6) / 1e9
+    tflops = grouped_flops(wl, T) / (us_layer * 1e-6) / 1e12
+    tc_peak = tensor_peak()
+    line = {
+        "metric": f"MoE grouped layer µs & achieved HBM GB/s at T={T}; tokens/s", "value": T * K * ws_n / (ms_max / 1e3),
+        "unit": "tokens/s", "n_gpus": ws_n, "steps": K, "warmup": W, "ms_per_step": ms_max / K,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded)", "config": {**config_of(wl), "T": T, "path": path,
+                                                 "mean_distinct_experts": sum(distinct) / L},
+        "us_per_layer": us_layer, "hbm_gbs": achieved, "hbm_frac_of_peak": achieved / peak,
+        "kernels_per_layer": kernels_per_layer,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "algorithmic_bytes_per_layer": alg, "peak_kind": f"{peak_kind} (hbm_gbs)",
+                     "tensor_tflops": tflops, "tensor_peak_tflops": tc_peak, "tensor_frac": tflops / tc_peak},
+        "gpu_launches": K * L * kernels_per_layer, "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def tensor_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"])
+    return 1900.0
 
 
 def main():
@@ -345,7 +460,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="sharded_decode",
-                    choices=["sharded_decode", "full_decode", "tiny"])
+                    choices=["sharded_decode", "full_decode", "tiny", "small_batch", "chunked_prefill"])
+    ap.add_argument("--T", type=int, default=None, help="tokens per step for the T > 1 workloads")
     ap.add_argument("--layers", type=int, default=None)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -358,6 +474,8 @@ def main():
     ws_n, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, wl, ws_n, rank)
+    elif wl.T > 1:
+        run_grouped(args, wl, ws_n, rank, local)
     else:
         run_ours(args, wl, ws_n, rank, local)
     if ws_n > 1:

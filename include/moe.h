@@ -100,7 +100,8 @@ typedef struct moe_cfg {
 } moe_cfg_t;
 
 /* cfg->flags bits selecting the T > 1 path.  With neither bit the library
- * uses the CUDA-core grouped kernels. */
+ * picks: the tcgen05 kernels when the shape allows (bf16, H % 128 == 0, I and
+ * Is multiples of 64), else the CUDA-core kernels. */
 #define MOE_FLAG_GROUPED_SIMT 1  /* T > 1 on the CUDA-core grouped kernels      */
 #define MOE_FLAG_GROUPED_TC 2    /* T > 1 on the tcgen05 grouped kernels;
                                     MOE_ERR_UNSUPPORTED if the shape does not allow it */

@@ -279,7 +279,7 @@ moe_status_t launch_grouped(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws,
   if (moe_status_t s = check_launch("group_kernel")) return s;
 
   const int sms = sm_count();
-  const bool use_tc = (c.flags & MOE_FLAG_GROUPED_TC) && L.tc_n > 0 && tc_path_supported(c);
+  const bool use_tc = !(c.flags & MOE_FLAG_GROUPED_SIMT) && L.tc_n > 0 && tc_path_supported(c);
   if ((c.flags & MOE_FLAG_GROUPED_TC) && !use_tc)
     return set_error(MOE_ERR_UNSUPPORTED, "grouped: the tensor-core path needs bf16, H %% 128 == 0, "
                                           "I and Is multiples of 64 and the TMA encoder");

@@ -18,6 +18,7 @@ namespace moe {
 constexpr int kRBM = 64;   // router rows (experts) per CTA tile
 constexpr int kRBN = 64;   // tokens per CTA tile
 constexpr int kRBK = 32;   // hidden elements per k-step
+constexpr int kRouterGemvMaxT = 64;  // T up to this uses the row-per-warp kernel
 
 template <int DT>
 __global__ void __launch_bounds__(256) router_logits_kernel(const uint8_t* __restrict__ x,
@@ -74,6 +75,77 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const uint8_t* __res
     }
 }
 
+// Small T: one warp per router row (held in registers as fp32, 2048 columns
+// per pass), dotted with a tile of up to 16 tokens staged in shared memory as
+// fp32.  Grid (ceil(E1 / 8), ceil(T / 16)).
+constexpr int kGvTok = 16;
+template <int DT>
+__global__ void __launch_bounds__(256) router_gemv_kernel(const uint8_t* __restrict__ x,
+                                                          const uint8_t* __restrict__ wr,
+                                                          const uint8_t* __restrict__ swg, int T, int H, int E,
+                                                          int E1, float* __restrict__ logits) {
+  extern __shared__ __align__(16) float xt[];  // [kGvTok][min(H, 2048)] fp32
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 8 + warp;
+  const int t0 = blockIdx.y * kGvTok;
+  const int nt = min(kGvTok, T - t0);
+  const size_t rowb = static_cast<size_t>(H) * 2;
+  const uint8_t* row = nullptr;
+  if (e < E) row = wr + static_cast<size_t>(e) * rowb;
+  else if (e == E && E1 > E) row = swg;
+  float acc[kGvTok];
+#pragma unroll
+  for (int t = 0; t < kGvTok; ++t) acc[t] = 0.f;
+  for (int k0 = 0; k0 < H; k0 += 2048) {
+    const int kw = min(2048, H - k0);
+    const int nch = kw >> 3;
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < nt * nch; idx += 256) {
+      const int t = idx / nch, c = idx - t * nch;
+      float f[8];
+      unpack8<DT>(ld_nc16(x + (static_cast<size_t>(t0 + t) * H + k0 + 8 * c) * 2), f);
+      float4* d = reinterpret_cast<float4*>(xt + static_cast<size_t>(t) * 2048 + 8 * c);
+      d[0] = make_float4(f[0], f[1], f[2], f[3]);
+      d[1] = make_float4(f[4], f[5], f[6], f[7]);
+    }
+    __syncthreads();
+    if (row) {
+      float w[8][8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int c = lane + 32 * q;
+        if (c < nch) unpack8<DT>(ld_stream16(row + (static_cast<size_t>(k0) + 8 * c) * 2), w[q]);
+        else
+#pragma unroll
+          for (int i = 0; i < 8; ++i) w[q][i] = 0.f;
+      }
+#pragma unroll
+      for (int t = 0; t < kGvTok; ++t) {
+        if (t < nt) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const int c = lane + 32 * q;
+            if (c < nch) {
+              const float4 a = reinterpret_cast<const float4*>(xt + static_cast<size_t>(t) * 2048)[2 * c];
+              const float4 b = reinterpret_cast<const float4*>(xt + static_cast<size_t>(t) * 2048)[2 * c + 1];
+              acc[t] = fmaf(w[q][0], a.x, acc[t]); acc[t] = fmaf(w[q][1], a.y, acc[t]);
+              acc[t] = fmaf(w[q][2], a.z, acc[t]); acc[t] = fmaf(w[q][3], a.w, acc[t]);
+              acc[t] = fmaf(w[q][4], b.x, acc[t]); acc[t] = fmaf(w[q][5], b.y, acc[t]);
+              acc[t] = fmaf(w[q][6], b.z, acc[t]); acc[t] = fmaf(w[q][7], b.w, acc[t]);
+            }
+          }
+        }
+      }
+    }
+  }
+  if (!row) return;
+#pragma unroll
+  for (int t = 0; t < kGvTok; ++t) {
+    const float v = warp_sum(acc[t]);
+    if (lane == 0 && t < nt) logits[static_cast<size_t>(t0 + t) * E1 + e] = v;
+  }
+}
+
 // One warp per token: rank, weights, outputs.
 template <int MAXM>
 __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restrict__ logits, int T, int E,
@@ -105,18 +177,28 @@ moe_status_t launch_router(const moe_cfg_t& c, const void* x, const void* router
   const int E1 = E + 1;
   float* lg = reinterpret_cast<float*>(ws + L.r_logits);
   const uint8_t* swg = c.has_shared_gate ? static_cast<const uint8_t*>(shared_gate_w) : nullptr;
-  dim3 g1((E1 + kRBM - 1) / kRBM, (T + kRBN - 1) / kRBN);
-  if (c.dtype == MOE_BF16)
-    router_logits_kernel<MOE_BF16><<<g1, 256, 0, st>>>(static_cast<const uint8_t*>(x),
-                                                       static_cast<const uint8_t*>(router_w), swg, T,
-                                                       c.hidden, E, swg ? E1 : E, lg);
-  else
-    router_logits_kernel<MOE_F16><<<g1, 256, 0, st>>>(static_cast<const uint8_t*>(x),
-                                                      static_cast<const uint8_t*>(router_w), swg, T,
-                                                      c.hidden, E, swg ? E1 : E, lg);
+  const int stride = swg ? E1 : E;
+  const uint8_t* xb = static_cast<const uint8_t*>(x);
+  const uint8_t* wb = static_cast<const uint8_t*>(router_w);
+  if (T <= kRouterGemvMaxT) {
+    dim3 gg((E1 + 7) / 8, (T + kGvTok - 1) / kGvTok);
+    const size_t sm = static_cast<size_t>(kGvTok) * 2048 * 4;
+    if (c.dtype == MOE_BF16) {
+      cudaFuncSetAttribute(router_gemv_kernel<MOE_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+      router_gemv_kernel<MOE_BF16><<<gg, 256, sm, st>>>(xb, wb, swg, T, c.hidden, E, stride, lg);
+    } else {
+      cudaFuncSetAttribute(router_gemv_kernel<MOE_F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+      router_gemv_kernel<MOE_F16><<<gg, 256, sm, st>>>(xb, wb, swg, T, c.hidden, E, stride, lg);
+    }
+  } else {
+    dim3 g1((E1 + kRBM - 1) / kRBM, (T + kRBN - 1) / kRBN);
+    if (c.dtype == MOE_BF16)
+      router_logits_kernel<MOE_BF16><<<g1, 256, 0, st>>>(xb, wb, swg, T, c.hidden, E, stride, lg);
+    else
+      router_logits_kernel<MOE_F16><<<g1, 256, 0, st>>>(xb, wb, swg, T, c.hidden, E, stride, lg);
+  }
   if (moe_status_t s = check_launch("router_logits_kernel")) return s;
   // The logits rows are laid out with stride E1 only when the gate column exists.
-  const int stride = swg ? E1 : E;
   dim3 g2((T + 7) / 8);
   if (E <= 256)
     router_topk_kernel<8><<<g2, 256, 0, st>>>(lg, T, E, stride, c.top_k, c.norm_topk, ids, w, logits_out);

@@ -55,3 +55,12 @@ def test_two_rank_max_over_ranks():
         assert p.exitcode == 0
     res = sorted(q.get(timeout=5) for _ in range(2))
     assert res == [(0, 20.0), (1, 20.0)]
+
+
+def test_grouped_bytes_model():
+    wl = moe_synth.workload("small_batch")
+    # router + 10 distinct experts (W13 + W2) + shared (W13 + W2 + gate) + x and out for 4 tokens
+    H, E, I, Is = 2048, 256, 512, 512
+    expect = 2 * (E * H + 10 * 3 * I * H + 3 * Is * H + H) + 2 * 2 * 4 * H
+    assert bench.grouped_bytes(wl, 4, 10) == expect
+    assert bench.grouped_flops(wl, 1) == 2 * (E * H + 8 * 3 * I * H + 3 * Is * H)
