@@ -171,6 +171,62 @@ __device__ __forceinline__ void warp_topk(const float* vals, int n, int k, int* 
   }
 }
 
+// Compare-exchange of (key, index) pairs: afterwards (ka, ia) ranks first by
+// (key desc, index asc).
+__device__ __forceinline__ void ce_desc(uint32_t& ka, int& ia, uint32_t& kb, int& ib) {
+  const bool swap = kb > ka || (kb == ka && ib < ia);
+  const uint32_t tk = swap ? kb : ka;
+  const int ti = swap ? ib : ia;
+  kb = swap ? ka : kb;
+  ib = swap ? ia : ib;
+  ka = tk;
+  ia = ti;
+}
+
+// Top-k for n <= 256 values (same contract as warp_topk): each lane sorts its
+// 8 (key, index) pairs once with a 19-comparator network, then every round
+// takes the best lane head (redux max; lowest lane among equal heads, which
+// holds the lowest index) and that lane shifts its sorted list by one.
+__device__ __forceinline__ void warp_topk_sorted8(const float* vals, int n, int k, int* out_ids,
+                                                  float* out_vals) {
+  const int lane = threadIdx.x & 31;
+  const int m = (n + 31) >> 5;  // <= 8
+  uint32_t kk[8];
+  int ii[8];
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    const int idx = lane * m + s;
+    const bool in = s < m && idx < n;
+    kk[s] = in ? order_key(vals[idx]) : 0u;
+    ii[s] = in ? idx : 0x7fffffff;
+  }
+  // optimal 8-input sorting network (19 comparators), descending
+  ce_desc(kk[0], ii[0], kk[2], ii[2]); ce_desc(kk[1], ii[1], kk[3], ii[3]);
+  ce_desc(kk[4], ii[4], kk[6], ii[6]); ce_desc(kk[5], ii[5], kk[7], ii[7]);
+  ce_desc(kk[0], ii[0], kk[4], ii[4]); ce_desc(kk[1], ii[1], kk[5], ii[5]);
+  ce_desc(kk[2], ii[2], kk[6], ii[6]); ce_desc(kk[3], ii[3], kk[7], ii[7]);
+  ce_desc(kk[0], ii[0], kk[1], ii[1]); ce_desc(kk[2], ii[2], kk[3], ii[3]);
+  ce_desc(kk[4], ii[4], kk[5], ii[5]); ce_desc(kk[6], ii[6], kk[7], ii[7]);
+  ce_desc(kk[2], ii[2], kk[4], ii[4]); ce_desc(kk[3], ii[3], kk[5], ii[5]);
+  ce_desc(kk[1], ii[1], kk[4], ii[4]); ce_desc(kk[3], ii[3], kk[6], ii[6]);
+  ce_desc(kk[1], ii[1], kk[2], ii[2]); ce_desc(kk[3], ii[3], kk[4], ii[4]);
+  ce_desc(kk[5], ii[5], kk[6], ii[6]);
+  for (int r = 0; r < k; ++r) {
+    const uint32_t mx = __reduce_max_sync(0xffffffffu, kk[0]);
+    const uint32_t ball = __ballot_sync(0xffffffffu, kk[0] == mx && ii[0] != 0x7fffffff);
+    const int winner = __ffs(ball) - 1;
+    if (lane == winner) {
+      out_ids[r] = ii[0];
+      out_vals[r] = vals[ii[0]];
+#pragma unroll
+      for (int s = 0; s < 7; ++s) { kk[s] = kk[s + 1]; ii[s] = ii[s + 1]; }
+      kk[7] = 0u;
+      ii[7] = 0x7fffffff;
+    }
+  }
+  __syncwarp();
+}
+
 // Routing weights for the k selected logits (sel[0] is the largest).  With
 // norm_topk: softmax over the k selected logits, which equals the full
 // softmax renormalised over the k.  Without: exp(l - max) / sum over all n.

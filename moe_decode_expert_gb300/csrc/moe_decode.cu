@@ -109,13 +109,14 @@ struct RowPair {
   }
 };
 
-// Dot of one W2 row (n 2-byte elements in smem) with n fp32 activations,
-// lane-strided over 16-byte chunks; returns this lane's partial sum.
+// Dot of one W2 row (n 2-byte elements in smem) with n fp32 activations by a
+// team of 16 threads (tl = 0..15), each taking every 16th 16-byte chunk;
+// returns this thread's partial sum.
 template <int DT>
-__device__ __forceinline__ float smem_row_dot(const uint8_t* row, const float* act, int n, int lane) {
+__device__ __forceinline__ float smem_row_dot16(const uint8_t* row, const float* act, int n, int tl) {
   float acc = 0.f;
   const int nch = n >> 3;
-  for (int c = lane; c < nch; c += 32) {
+  for (int c = tl; c < nch; c += 16) {
     const uint4 v = *reinterpret_cast<const uint4*>(row + 16 * c);
     const float4 xa = reinterpret_cast<const float4*>(act)[2 * c];
     const float4 xb = reinterpret_cast<const float4*>(act)[2 * c + 1];
@@ -221,7 +222,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_fused_kernel(const Deco
     const bool ok = ll_gather(a.ll_logits, lg, nl, lane, 32, epoch, global_ns() + a.timeout_ns);
     if (__all_sync(0xffffffffu, ok)) {
       __syncwarp();
-      if (E <= 256) warp_topk<8>(lg, E, k, s_ids, s_sel);
+      if (E <= 256) warp_topk_sorted8(lg, E, k, s_ids, s_sel);
       else warp_topk<32>(lg, E, k, s_ids, s_sel);
       __syncwarp();
       warp_routing_weights(lg, E, s_sel, k, a.norm_topk, s_w);
@@ -271,18 +272,30 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_fused_kernel(const Deco
     if (tid == 0 && !mbar_wait_until(&bar, 0, global_ns() + a.timeout_ns)) s_fail = kDevTimeoutCopy;
     __syncthreads();
     if (!s_fail) {
-      for (int r = warp; r < hn; r += kDecWarps) {
+      // Teams of 16 threads, one output row per team; each thread covers a
+      // 1/16 slice of every expert's row with independent partial sums, so
+      // the k+1 short dot products run in parallel instead of one after another.
+      // A warp holds two teams (rows rbase, rbase + 1); the loop bound is
+      // warp-uniform so every lane reaches the shuffles.
+      const int tl = tid & 15;
+      for (int rbase = warp * 2; rbase < hn; rbase += kDecThreads / 16) {
+        const int r = rbase + ((tid >> 4) & 1);
+        const bool active = r < hn;
         float acc = 0.f;
-        for (int j = 0; j < k; ++j) {
-          const uint8_t* row = w2s + (static_cast<size_t>(j) * hn + r) * I * 2;
-          acc = fmaf(s_w[j], smem_row_dot<DT>(row, acts + static_cast<size_t>(j) * I, I, lane), acc);
+        if (active) {
+#pragma unroll 4
+          for (int j = 0; j < k; ++j) {
+            const uint8_t* row = w2s + (static_cast<size_t>(j) * hn + r) * I * 2;
+            acc = fmaf(s_w[j], smem_row_dot16<DT>(row, acts + static_cast<size_t>(j) * I, I, tl), acc);
+          }
+          if (Is > 0) {
+            const uint8_t* row = w2s + (static_cast<size_t>(k) * hn * I + static_cast<size_t>(r) * Is) * 2;
+            acc = fmaf(s_gate, smem_row_dot16<DT>(row, acts + P, Is, tl), acc);
+          }
         }
-        if (Is > 0) {
-          const uint8_t* row = w2s + (static_cast<size_t>(k) * hn * I + static_cast<size_t>(r) * Is) * 2;
-          acc = fmaf(s_gate, smem_row_dot<DT>(row, acts + P, Is, lane), acc);
-        }
-        acc = warp_sum(acc);
-        if (lane == 0) store_out(a.out, h0 + r, acc, a.out_dtype);
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (active && tl == 0) store_out(a.out, h0 + r, acc, a.out_dtype);
       }
       // Every CTA has read the epoch before publishing its activations and CTA 0
       // has now seen all of them, so the next launch may use the next epoch.

@@ -34,7 +34,7 @@ constexpr int kHB = 64;           // output rows per w2 work item
 __global__ void __launch_bounds__(1024) group_kernel(const int32_t* __restrict__ ids, int T, int k, int E,
                                                      int has_shared, int32_t* counts_out,
                                                      int32_t* offsets, int32_t* perm, int32_t* tiles,
-                                                     Control* ctrl) {
+                                                     int write_tiles, Control* ctrl) {
   __shared__ int32_t cnt[1025 + 1];
   __shared__ int32_t cur[1025 + 1];
   __shared__ int32_t tcnt[1025 + 1];
@@ -88,16 +88,24 @@ __global__ void __launch_bounds__(1024) group_kernel(const int32_t* __restrict__
   for (int e = tid; e < n; e += 1024) {
     offsets[e] = cur[e];
     counts_out[e] = cnt[e];
-    const int nt = (cnt[e] + kTN - 1) / kTN;
-    for (int tt = 0; tt < nt; ++tt) {
-      tiles[2 * (tcnt[e] + tt)] = e;
-      tiles[2 * (tcnt[e] + tt) + 1] = cur[e] + tt * kTN;
-    }
   }
+  const unsigned long long tot = wtot[31];
+  const int n_tiles = static_cast<int>(tot & 0xffffffffu);
   if (tid == 0) {
-    const unsigned long long tot = wtot[31];
     offsets[n] = static_cast<int>(tot >> 32);
-    counts_out[n] = static_cast<int>(tot & 0xffffffffu);  // number of tiles
+    counts_out[n] = n_tiles;  // number of tiles
+  }
+  if (write_tiles) {
+    // tile i belongs to the last expert whose first tile index is <= i
+    for (int i = tid; i < n_tiles; i += 1024) {
+      int lo = 0, hi = n - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (tcnt[mid] <= i) lo = mid; else hi = mid - 1;
+      }
+      tiles[2 * i] = lo;
+      tiles[2 * i + 1] = cur[lo] + (i - tcnt[lo]) * kTN;
+    }
   }
   __syncthreads();
   // File routed pairs (any order within an expert) and the shared pairs (in token order).
@@ -275,11 +283,11 @@ moe_status_t launch_grouped(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws,
   const int gate_stride = c.has_shared_gate ? E + 1 : E;
   const int Imax = I > Is ? I : Is;
 
-  group_kernel<<<1, 1024, 0, st>>>(p.topk_ids, T, k, E, Is > 0, counts, offsets, perm, tiles, ctrl);
+  const bool use_tc = !(c.flags & MOE_FLAG_GROUPED_SIMT) && L.tc_n > 0 && tc_path_supported(c);
+  group_kernel<<<1, 1024, 0, st>>>(p.topk_ids, T, k, E, Is > 0, counts, offsets, perm, tiles, use_tc ? 0 : 1, ctrl);
   if (moe_status_t s = check_launch("group_kernel")) return s;
 
   const int sms = sm_count();
-  const bool use_tc = !(c.flags & MOE_FLAG_GROUPED_SIMT) && L.tc_n > 0 && tc_path_supported(c);
   if ((c.flags & MOE_FLAG_GROUPED_TC) && !use_tc)
     return set_error(MOE_ERR_UNSUPPORTED, "grouped: the tensor-core path needs bf16, H %% 128 == 0, "
                                           "I and Is multiples of 64 and the TMA encoder");

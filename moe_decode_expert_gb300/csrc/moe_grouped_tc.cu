@@ -462,6 +462,152 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
+
+// ======================================================== router GEMM (large T)
+// logits[t, e] = x[t] . Wr[e] for T tokens on tcgen05: router rows are M (128
+// per tile), tokens N (128), K = H.  M-tiles [0, mE) cover the E router rows;
+// with a shared gate one more M-tile reads the gate vector as a one-row tensor
+// (TMA fills the other 127 rows with zeros).  Tile t: m = t % nm, n = t / nm.
+template <int DT, int N>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    tc_router_kernel(const __grid_constant__ CUtensorMap mapWr, const __grid_constant__ CUtensorMap mapG,
+                     const __grid_constant__ CUtensorMap mapX, int T, int H, int E, int E1, int mE, int nm,
+                     float* __restrict__ logits, Control* ctrl, uint64_t timeout) {
+  constexpr uint32_t kStage = kTileA + N * 128;
+  constexpr int kStages = kSmemBudget / kStage > 8 ? 8 : kSmemBudget / kStage;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t full[kStages], empty[kStages], tfull[2], tempty[2], done;
+  __shared__ uint32_t tmem_base_s;
+  __shared__ volatile int s_abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], 4); }
+    mbar_init(&done, 1);
+    mbar_fence_init();
+    s_abort = 0;
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_s, 2 * N);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tmem_base_s;
+  const int ntiles = nm * ((T + N - 1) / N);
+  const int KB = H / kBK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, issued_phase = 0;
+      for (int t = blockIdx.x; t < ntiles && !s_abort; t += gridDim.x) {
+        const int m = t % nm, n = t / nm;
+        const bool gate = m >= mE;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!tc_wait(&empty[stage], phase ^ 1u, timeout, &s_abort)) {
+            s_abort = 1;
+            report_error(ctrl, kDevTimeoutCopy, blockIdx.x);
+            break;
+          }
+          uint8_t* sA = smem + stage * kStage;
+          mbar_arrive_expect_tx(&full[stage], kStage);
+          tma_load_2d(sA, gate ? &mapG : &mapWr, &full[stage], kb * kBK, gate ? 0 : m * 128);
+          tma_load_2d(sA + kTileA, &mapX, &full[stage], kb * kBK, n * N);
+          issued_mask |= 1u << stage;
+          issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      for (int s = 0; s < kStages; ++s)
+        if (issued_mask & (1u << s)) mbar_wait_until(&full[s], (issued_phase >> s) & 1u, global_ns() + timeout);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16<DT, N>();
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      for (int t = blockIdx.x; t < ntiles && !s_abort; t += gridDim.x, ++it) {
+        const int acc = it & 1;
+        if (!tc_wait(&tempty[acc], ((it >> 1) & 1) ^ 1u, timeout, &s_abort)) {
+          s_abort = 1;
+          report_error(ctrl, kDevTimeoutCopy, blockIdx.x);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tbase + static_cast<uint32_t>(acc * N);
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!tc_wait(&full[stage], phase, timeout, &s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sA = smem_u32(smem + stage * kStage);
+          const uint32_t sB = sA + kTileA;
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            tc_mma(d, sw128_desc(sA + 32 * k), sw128_desc(sB + 32 * k), idesc, (kb | k) != 0);
+          tc_commit(&empty[stage]);
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) {
+          s_abort = 1;
+          report_error(ctrl, kDevTimeoutCopy, blockIdx.x);
+          break;
+        }
+        tc_commit(&tfull[acc]);
+      }
+      tc_commit(&done);
+      mbar_wait_until(&done, 0, global_ns() + timeout);
+    }
+  } else {
+    const int q = warp & 3;
+    const int row = 32 * q + lane;
+    int it = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+      const int m = t % nm, n = t / nm;
+      const int acc = it & 1;
+      const bool ok = !s_abort && tc_wait(&tfull[acc], (it >> 1) & 1, timeout, &s_abort);
+      if (epi_any(!ok)) {
+        s_abort = 1;
+        report_error(ctrl, kDevTimeoutCopy, blockIdx.x);
+        break;
+      }
+      tc_fence_after();
+      const bool gate = m >= mE;
+      const int e = gate ? E : m * 128 + row;
+      const bool write = gate ? row == 0 : e < E;
+      for (int c0 = 0; c0 < N; c0 += 16) {
+        if (n * N + c0 >= T) break;
+        float v[16];
+        tmem_ld16(tbase + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(acc * N + c0), v);
+        if (write) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int tok = n * N + c0 + j;
+            if (tok < T) logits[static_cast<size_t>(tok) * E1 + e] = v[j];
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 2 * N);
+  }
+}
+
 // ===================================================== schedule + gather
 // Tile lists of both passes from the per-expert counts/offsets (one CTA).
 // Layout of `sched`: [0] n13, [1] n2, then TcTile arrays at the offsets given.
@@ -470,16 +616,17 @@ __global__ void __launch_bounds__(1024) tc_schedule_kernel(const int32_t* __rest
                                                            int Is, int H, int N, int32_t* n13, int32_t* n2,
                                                            TcTile* t13, TcTile* t2) {
   __shared__ unsigned long long wtot[32];
+  __shared__ int pre13[1026], pre2[1026];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n = E + 1;
-  // one expert per thread (n <= 1025: two per thread at most)
-  int a13[2] = {0, 0}, a2[2] = {0, 0}, cnt[2] = {0, 0};
+  // tiles of each expert (two experts per thread; n <= 1025)
+  int a13[2] = {0, 0}, a2[2] = {0, 0};
   for (int s = 0; s < 2; ++s) {
     const int e = 2 * tid + s;
     if (e < n) {
-      cnt[s] = counts[e];
+      const int cnt = counts[e];
       const int ie = e == E ? Is : I;
-      const int nt = (cnt[s] + N - 1) / N;
+      const int nt = (cnt + N - 1) / N;
       a13[s] = ie > 0 ? nt * (ie / 64) : 0;
       a2[s] = ie > 0 ? nt * (H / 128) : 0;
     }
@@ -504,29 +651,30 @@ __global__ void __launch_bounds__(1024) tc_schedule_kernel(const int32_t* __rest
   }
   __syncthreads();
   const unsigned long long before = incl - v + (warp ? wtot[warp - 1] : 0ull);
-  int b13 = static_cast<int>(before >> 32), b2 = static_cast<int>(before & 0xffffffffu);
-  for (int s = 0; s < 2; ++s) {
-    const int e = 2 * tid + s;
-    if (e >= n || cnt[s] == 0) {
-      b13 += a13[s];
-      b2 += a2[s];
-      continue;
+  const int b13 = static_cast<int>(before >> 32), b2 = static_cast<int>(before & 0xffffffffu);
+  if (2 * tid < n) { pre13[2 * tid] = b13; pre2[2 * tid] = b2; }
+  if (2 * tid + 1 < n) { pre13[2 * tid + 1] = b13 + a13[0]; pre2[2 * tid + 1] = b2 + a2[0]; }
+  __syncthreads();
+  const int tot13 = static_cast<int>(wtot[31] >> 32), tot2 = static_cast<int>(wtot[31] & 0xffffffffu);
+  if (tid == 0) { *n13 = tot13; *n2 = tot2; }
+  // Fill both lists in parallel: tile i belongs to the last expert whose first
+  // tile index is <= i (experts without tiles share their successor's start).
+  for (int i = tid; i < tot13 + tot2; i += 1024) {
+    const bool second = i >= tot13;
+    const int ii = second ? i - tot13 : i;
+    const int* pre = second ? pre2 : pre13;
+    int lo = 0, hi = n - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pre[mid] <= ii) lo = mid; else hi = mid - 1;
     }
+    const int e = lo;
     const int ie = e == E ? Is : I;
-    const int nt = (cnt[s] + N - 1) / N;
-    const int m13 = ie / 64, m2 = H / 128;
-    for (int j = 0; j < nt; ++j) {
-      const int pos0 = offsets[e] + j * N;
-      const int nv = min(N, cnt[s] - j * N);
-      for (int mm = 0; mm < m13; ++mm) t13[b13 + j * m13 + mm] = TcTile{e, mm, pos0, nv};
-      for (int mm = 0; mm < m2; ++mm) t2[b2 + j * m2 + mm] = TcTile{e, mm, pos0, nv};
-    }
-    b13 += a13[s];
-    b2 += a2[s];
-  }
-  if (tid == 0) {
-    *n13 = static_cast<int>(wtot[31] >> 32);
-    *n2 = static_cast<int>(wtot[31] & 0xffffffffu);
+    const int per_n = second ? H / 128 : ie / 64;  // M-tiles per N-tile
+    const int j = (ii - pre[e]) / per_n, mm = (ii - pre[e]) - j * per_n;
+    const int cnt = counts[e];
+    const TcTile tl{e, mm, offsets[e] + j * N, min(N, cnt - j * N)};
+    if (second) t2[ii] = tl; else t13[ii] = tl;
   }
 }
 
@@ -653,6 +801,37 @@ static moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uin
                                                                I, Is, E, k, y, ctrl, timeout);
   if (moe_status_t s = check_launch("tc_w2_kernel")) return s;
   stat_kernels(4);
+  return MOE_OK;
+}
+
+
+bool tc_router_supported(const moe_cfg_t& c) {
+  return c.dtype == MOE_BF16 && c.hidden % 64 == 0 && encode_fn() != nullptr;
+}
+
+// logits [T, E1] (E1 = E, or E + 1 with the gate column) on tensor cores.
+moe_status_t launch_tc_router(const moe_cfg_t& c, const void* x, const void* router_w, const void* gate_w,
+                              int32_t T, float* logits, int E1, Control* ctrl, cudaStream_t st) {
+  constexpr int DT = MOE_BF16, N = 128;
+  const int H = c.hidden, E = c.n_experts;
+  const int mE = (E + 127) / 128;
+  const int nm = mE + (gate_w ? 1 : 0);
+  CUtensorMap mWr, mG, mX;
+  bool ok = make_map(&mWr, DT, router_w, H, E, static_cast<uint64_t>(H) * 2, 128) &&
+            make_map(&mG, DT, gate_w ? gate_w : router_w, H, 1, static_cast<uint64_t>(H) * 2, 128) &&
+            make_map(&mX, DT, x, H, T, static_cast<uint64_t>(H) * 2, N);
+  if (!ok) return set_error(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (router)");
+  constexpr uint32_t st_bytes = kTileA + N * 128;
+  constexpr int ns = kSmemBudget / st_bytes > 8 ? 8 : kSmemBudget / st_bytes;
+  const size_t smem = static_cast<size_t>(ns) * st_bytes + 1024;
+  cudaFuncSetAttribute(tc_router_kernel<DT, N>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  const int tiles = nm * ((T + N - 1) / N);
+  const int sms = sm_count();
+  const int g = tiles < sms ? tiles : sms;
+  tc_router_kernel<DT, N><<<g, kTcThreads, smem, st>>>(mWr, mG, mX, T, H, E, E1, mE, nm, logits, ctrl,
+                                                       wait_timeout_ns());
+  if (moe_status_t s = check_launch("tc_router_kernel")) return s;
+  stat_kernels(1);
   return MOE_OK;
 }
 

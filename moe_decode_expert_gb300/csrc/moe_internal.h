@@ -88,6 +88,10 @@ moe_status_t launch_wait_test(uint8_t* ws, cudaStream_t st);
 bool tc_shape_ok(const moe_cfg_t& c);        // shape/dtype eligibility (host only)
 bool tc_path_supported(const moe_cfg_t& c);  // eligibility and the TMA encoder is available
 int tc_tile_n(const moe_cfg_t& c, int32_t T);
+struct Control;
+bool tc_router_supported(const moe_cfg_t& c);
+moe_status_t launch_tc_router(const moe_cfg_t& c, const void* x, const void* router_w, const void* gate_w,
+                              int32_t T, float* logits, int E1, Control* ctrl, cudaStream_t st);
 moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws, const WsLayout& L, int32_t T,
                               cudaStream_t st);
 

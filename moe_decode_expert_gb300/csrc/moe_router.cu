@@ -19,6 +19,7 @@ constexpr int kRBM = 64;   // router rows (experts) per CTA tile
 constexpr int kRBN = 64;   // tokens per CTA tile
 constexpr int kRBK = 32;   // hidden elements per k-step
 constexpr int kRouterGemvMaxT = 64;  // T up to this uses the row-per-warp kernel
+constexpr int kRouterTcMinT = 256;   // bf16 and T from this on: tensor-core router
 
 template <int DT>
 __global__ void __launch_bounds__(256) router_logits_kernel(const uint8_t* __restrict__ x,
@@ -158,7 +159,8 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
   const float* row = logits + static_cast<size_t>(t) * E1;
-  warp_topk<MAXM>(row, E, k, s_ids[warp], s_sel[warp]);
+  if constexpr (MAXM == 8) warp_topk_sorted8(row, E, k, s_ids[warp], s_sel[warp]);
+  else warp_topk<MAXM>(row, E, k, s_ids[warp], s_sel[warp]);
   __syncwarp();
   warp_routing_weights(row, E, s_sel[warp], k, norm_topk, s_w[warp]);
   __syncwarp();
@@ -180,7 +182,12 @@ moe_status_t launch_router(const moe_cfg_t& c, const void* x, const void* router
   const int stride = swg ? E1 : E;
   const uint8_t* xb = static_cast<const uint8_t*>(x);
   const uint8_t* wb = static_cast<const uint8_t*>(router_w);
-  if (T <= kRouterGemvMaxT) {
+  const bool tc = T >= kRouterTcMinT && tc_router_supported(c);
+  if (tc) {
+    if (moe_status_t s = launch_tc_router(c, x, router_w, swg, T, lg, stride,
+                                          reinterpret_cast<Control*>(ws + L.ctrl), st))
+      return s;
+  } else if (T <= kRouterGemvMaxT) {
     dim3 gg((E1 + 7) / 8, (T + kGvTok - 1) / kGvTok);
     const size_t sm = static_cast<size_t>(kGvTok) * 2048 * 4;
     if (c.dtype == MOE_BF16) {
