@@ -223,7 +223,10 @@ def run_ours(args, wl, ws_n, rank, local):
 
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
-    cfg = m.cfg_from_workload(wl)
+    # Fixed inference weights: nothing on the stream writes them, so each layer
+    # kernel may start reading its routing-independent weights before it waits
+    # for the previous layer (x is still read only after that wait).
+    cfg = m.cfg_from_workload(wl, None, 0 if args.no_static_weights else m.MOE_FLAG_STATIC_WEIGHTS)
     L = wl.layers
     H, k = wl.hidden, wl.top_k
     layers = [moe_synth.make_layer(wl, l, 1, device=dev, weights_only=True) for l in range(L)]
@@ -233,6 +236,7 @@ def run_ours(args, wl, ws_n, rank, local):
     wts = torch.empty(L, 1, k, dtype=torch.float32, device=dev)
     ws = m.alloc_workspace(cfg, 1, dev)
     stream = torch.cuda.Stream(device=dev)
+    stream.wait_stream(torch.cuda.current_stream(dev))  # inputs were generated on the default stream
 
     def step(s):
         for l in range(L):
@@ -332,7 +336,7 @@ def run_ours(args, wl, ws_n, rank, local):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws_n, "steps": K, "warmup": W,
         "ms_per_step": ms_max / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16" if wl.dtype == 1 else "bf16", "data": "synthetic (seeded N(0,0.02) weights, N(0,1) x)",
-        "config": config_of(wl),
+        "config": {**config_of(wl), "static_weights_flag": not args.no_static_weights},
         "us_per_layer": us_layer,
         "hbm_gbs": achieved,
         "hbm_frac_of_peak": achieved / peak,
@@ -381,6 +385,7 @@ def run_grouped(args, wl, ws_n, rank, local):
     wts = torch.empty(L, T, k, dtype=torch.float32, device=dev)
     ws = m.alloc_workspace(cfg, T, dev)
     stream = torch.cuda.Stream(device=dev)
+    stream.wait_stream(torch.cuda.current_stream(dev))  # inputs were generated on the default stream
 
     def step():
         for l in range(L):
@@ -465,6 +470,8 @@ def main():
     ap.add_argument("--layers", type=int, default=None)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-static-weights", action="store_true",
+                    help="T=1: do not let layer kernels read weights before the previous layer completes")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -105,6 +105,13 @@ typedef struct moe_cfg {
 #define MOE_FLAG_GROUPED_SIMT 1  /* T > 1 on the CUDA-core grouped kernels      */
 #define MOE_FLAG_GROUPED_TC 2    /* T > 1 on the tcgen05 grouped kernels;
                                     MOE_ERR_UNSUPPORTED if the shape does not allow it */
+#define MOE_FLAG_STATIC_WEIGHTS 4 /* promise: no work still in flight on the stream
+                                    when the call is enqueued writes any weight
+                                    tensor (fixed inference weights).  The T = 1
+                                    kernel may then start reading its
+                                    routing-independent weights (router rows,
+                                    shared expert) before it waits for the
+                                    preceding kernel; x is always read after. */
 
 /* Caller-owned routing outputs, [T, k] each (device memory). */
 typedef struct moe_topk {

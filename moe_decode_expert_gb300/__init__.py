@@ -57,6 +57,7 @@ class moe_stats_t(ctypes.Structure):
 
 MOE_FLAG_GROUPED_SIMT = 1
 MOE_FLAG_GROUPED_TC = 2
+MOE_FLAG_STATIC_WEIGHTS = 4
 
 
 @dataclass(frozen=True)

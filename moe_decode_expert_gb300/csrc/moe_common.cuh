@@ -33,7 +33,8 @@ struct Control {
   uint32_t detail;     // CTA (or token) that recorded it
   uint32_t gen;        // epoch of the last single-launch decode on this workspace
   uint32_t never_set;  // a flag no kernel writes (failure-path test)
-  uint32_t pad[60];
+  uint32_t arrive[2];  // CTAs done publishing activations, by launch-epoch parity
+  uint32_t pad[58];
 };
 static_assert(sizeof(Control) == 256, "control block is 256 bytes");
 
@@ -187,8 +188,15 @@ __device__ __forceinline__ void ce_desc(uint32_t& ka, int& ia, uint32_t& kb, int
 // 8 (key, index) pairs once with a 19-comparator network, then every round
 // takes the best lane head (redux max; lowest lane among equal heads, which
 // holds the lowest index) and that lane shifts its sorted list by one.
+struct NoSelectHook {
+  __device__ __forceinline__ void operator()(int) const {}
+};
+
+// `on_select(r)` is called by all lanes once out_ids[r] is written (after a
+// warp sync), so a caller can act on each expert while the ranking goes on.
+template <class Hook = NoSelectHook>
 __device__ __forceinline__ void warp_topk_sorted8(const float* vals, int n, int k, int* out_ids,
-                                                  float* out_vals) {
+                                                  float* out_vals, Hook on_select = Hook()) {
   const int lane = threadIdx.x & 31;
   const int m = (n + 31) >> 5;  // <= 8
   uint32_t kk[8];
@@ -223,6 +231,8 @@ __device__ __forceinline__ void warp_topk_sorted8(const float* vals, int n, int 
       kk[7] = 0u;
       ii[7] = 0x7fffffff;
     }
+    __syncwarp();
+    on_select(r);
   }
   __syncwarp();
 }

@@ -53,6 +53,7 @@ struct DecodeArgs {
   uint64_t* ll_logits;
   uint64_t* ll_act;
   int H, E, k, I, Is, has_gate, norm_topk, out_dtype;
+  int static_weights;  // MOE_FLAG_STATIC_WEIGHTS: weight reads may precede the PDL wait
   uint32_t off_lg, off_act, off_w2;
   uint64_t timeout_ns;
 };
@@ -109,27 +110,6 @@ struct RowPair {
   }
 };
 
-// Dot of one W2 row (n 2-byte elements in smem) with n fp32 activations by a
-// team of 16 threads (tl = 0..15), each taking every 16th 16-byte chunk;
-// returns this thread's partial sum.
-template <int DT>
-__device__ __forceinline__ float smem_row_dot16(const uint8_t* row, const float* act, int n, int tl) {
-  float acc = 0.f;
-  const int nch = n >> 3;
-  for (int c = tl; c < nch; c += 16) {
-    const uint4 v = *reinterpret_cast<const uint4*>(row + 16 * c);
-    const float4 xa = reinterpret_cast<const float4*>(act)[2 * c];
-    const float4 xb = reinterpret_cast<const float4*>(act)[2 * c + 1];
-    float f[8];
-    unpack8<DT>(v, f);
-    acc = fmaf(f[0], xa.x, acc); acc = fmaf(f[1], xa.y, acc);
-    acc = fmaf(f[2], xa.z, acc); acc = fmaf(f[3], xa.w, acc);
-    acc = fmaf(f[4], xb.x, acc); acc = fmaf(f[5], xb.y, acc);
-    acc = fmaf(f[6], xb.z, acc); acc = fmaf(f[7], xb.w, acc);
-  }
-  return acc;
-}
-
 template <int DT>
 __global__ void __launch_bounds__(kDecThreads, 2) decode_fused_kernel(const DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -141,6 +121,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_fused_kernel(const Deco
   __shared__ uint32_t s_epoch;
   __shared__ uint32_t s_fail;
   __shared__ int s_second_arrive_done;
+  __shared__ volatile int s_ready[32];  // slot r ranked (its id is in s_ids[r])
 
   float* xs = reinterpret_cast<float*>(smem);
   float* lg = reinterpret_cast<float*>(smem + a.off_lg);
@@ -160,12 +141,13 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_fused_kernel(const Deco
     mbar_fence_init();
     s_fail = 0;
     s_second_arrive_done = 0;
+    for (int r = 0; r < 32; ++r) s_ready[r] = 0;
   }
   pdl_launch_dependents();
   __syncthreads();
-  pdl_wait();  // x (and anything else an earlier kernel wrote) is visible from here
 
-  // ---- phase 1: routing-independent rows; the first round's loads go out before x is staged
+  // ---- phase 1: routing-independent rows; the first round's loads go out
+  // before x is staged (and, with static weights, before the PDL wait)
   const int n1 = E + a.has_gate + Is;
   int q = warp;
   int u = q * G + cta;
@@ -182,7 +164,21 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_fused_kernel(const Deco
       rp.two = 1;
     }
   };
-  if (u < n1) { setup_unit(u); rp.issue(0, nch, lane); }
+  auto issue_shared_w2 = [&]() {  // thread 0: the shared expert's W2 rows of this CTA's slice
+    if (Is > 0 && hn > 0) {
+      const uint32_t bytes = static_cast<uint32_t>(hn) * Is * 2;
+      mbar_arrive_expect_tx(&bar, bytes);
+      bulk_g2s(w2s + static_cast<size_t>(k) * hn * I * 2, a.sw2 + static_cast<size_t>(h0) * Is * 2, bytes, &bar);
+    } else {
+      mbar_arrive(&bar);
+    }
+  };
+  if (a.static_weights) {
+    if (u < n1) { setup_unit(u); rp.issue(0, nch, lane); }
+    if (tid == 0) issue_shared_w2();
+  }
+  pdl_wait();  // x (and anything else an earlier kernel wrote) is visible from here
+  if (!a.static_weights && u < n1) { setup_unit(u); rp.issue(0, nch, lane); }
 
   for (int c = tid; c < nch; c += kDecThreads) {
     float f[8];
@@ -193,13 +189,10 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_fused_kernel(const Deco
   if (tid == 0) {
     uint32_t ep = ld_relaxed_u32(&a.ctrl->gen) + 1u;
     s_epoch = ep ? ep : 1u;
-    if (Is > 0 && hn > 0) {  // shared expert's W2 rows of this CTA's slice
-      const uint32_t bytes = static_cast<uint32_t>(hn) * Is * 2;
-      mbar_arrive_expect_tx(&bar, bytes);
-      bulk_g2s(w2s + static_cast<size_t>(k) * hn * I * 2, a.sw2 + static_cast<size_t>(h0) * Is * 2, bytes, &bar);
-    } else {
-      mbar_arrive(&bar);
-    }
+    // The arrival counter of the other parity was last used by the previous
+    // launch, which has completed; clear it for the next launch.
+    if (cta == 0) atomicExch(&a.ctrl->arrive[(s_epoch + 1u) & 1u], 0u);
+    if (!a.static_weights) issue_shared_w2();
   }
   __syncthreads();
   const uint32_t epoch = s_epoch;
@@ -216,86 +209,156 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_fused_kernel(const Deco
     if (u < n1) { setup_unit(u); rp.issue(0, nch, lane); }
   }
 
-  // ---- phase 2: gather the logits, rank, weights (warp 0)
+  // ---- phase 2 (warp 0): gather the logits and rank them.  Each ranked
+  // expert is published to the other warps, and its W2 rows requested, as
+  // soon as its round ends, so expert loads overlap the rest of the ranking.
   if (warp == 0) {
     const int nl = E + a.has_gate;
     const bool ok = ll_gather(a.ll_logits, lg, nl, lane, 32, epoch, global_ns() + a.timeout_ns);
     if (__all_sync(0xffffffffu, ok)) {
+      const uint32_t bytes = static_cast<uint32_t>(hn) * I * 2;
+      if (lane == 0) {
+        if (hn > 0) mbar_arrive_expect_tx(&bar, bytes * k);
+        else mbar_arrive(&bar);
+        s_second_arrive_done = 1;
+      }
       __syncwarp();
-      if (E <= 256) warp_topk_sorted8(lg, E, k, s_ids, s_sel);
-      else warp_topk<32>(lg, E, k, s_ids, s_sel);
+      auto publish = [&](int r) {
+        if (lane == 0) {
+          __threadfence_block();
+          s_ready[r] = 1;
+        }
+      };
+      if (E <= 256) {
+        warp_topk_sorted8(lg, E, k, s_ids, s_sel, publish);
+      } else {
+        warp_topk<32>(lg, E, k, s_ids, s_sel);
+        __syncwarp();
+        for (int r = 0; r < k; ++r) publish(r);
+      }
       __syncwarp();
+      // this CTA's W2 rows of the k experts, one lane per expert
+      if (hn > 0 && lane < k)
+        bulk_g2s(w2s + static_cast<size_t>(lane) * hn * I * 2,
+                 a.w2 + (static_cast<size_t>(s_ids[lane]) * H + h0) * I * 2, bytes, &bar);
       warp_routing_weights(lg, E, s_sel, k, a.norm_topk, s_w);
       if (lane == 0) s_gate = a.has_gate ? sigmoid_f(lg[E]) : 1.0f;
+      __syncwarp();
+      if (cta == 0 && lane < k) {
+        a.topk_ids[lane] = s_ids[lane];
+        a.topk_w[lane] = s_w[lane];
+      }
     } else if (lane == 0) {
       s_fail = kDevTimeoutLogits;
+      __threadfence_block();
+      for (int r = 0; r < 32; ++r) s_ready[r] = 1;  // let the waiting warps see the failure
     }
   }
-  __syncthreads();
 
-  if (!s_fail) {
-    // ---- phase 3: W2 rows of this CTA's slice (bulk copies), routed W13 pairs (registers)
-    if (tid == 0) {
-      if (hn > 0) {
-        const uint32_t bytes = static_cast<uint32_t>(hn) * I * 2;
-        mbar_arrive_expect_tx(&bar, bytes * k);
-        for (int j = 0; j < k; ++j)
-          bulk_g2s(w2s + static_cast<size_t>(j) * hn * I * 2,
-                   a.w2 + (static_cast<size_t>(s_ids[j]) * H + h0) * I * 2, bytes, &bar);
-      } else {
-        mbar_arrive(&bar);
-      }
-      s_second_arrive_done = 1;
+  // ---- phase 3: this CTA's share of the k*I routed gate/up pairs; a warp
+  // starts a pair as soon as the pair's expert has been ranked.
+  const int P = k * I;
+  for (int qq = warp;; qq += kDecWarps) {
+    const int p = qq * G + cta;
+    if (p >= P) break;
+    const int j = p / I, i = p - j * I;
+    const uint64_t deadline = global_ns() + a.timeout_ns;
+    bool ready = true;
+    while (s_ready[j] == 0) {
+      if (global_ns() > deadline) { ready = false; break; }
+      __nanosleep(32);
     }
-    if (cta == 0 && tid < k) {
-      a.topk_ids[tid] = s_ids[tid];
-      a.topk_w[tid] = s_w[tid];
+    __threadfence_block();
+    if (!ready) {
+      if (lane == 0) s_fail = kDevTimeoutLogits;
+      break;
     }
-    const int P = k * I;
-    for (int qq = warp;; qq += kDecWarps) {
-      const int p = qq * G + cta;
-      if (p >= P) break;
-      const int j = p / I, i = p - j * I;
-      const size_t erow = static_cast<size_t>(s_ids[j]) * 2 * I;
-      rp.r0 = a.w13 + (erow + i) * rowb;
-      rp.r1 = a.w13 + (erow + I + i) * rowb;
-      rp.two = 1;
-      rp.issue(0, nch, lane);
-      float g, up;
-      rp.finish(xs, nch, lane, g, up);
-      if (lane == 0) ll_store(a.ll_act + p, silu_f(g) * up, epoch);
-    }
+    if (s_fail) break;
+    const size_t erow = static_cast<size_t>(s_ids[j]) * 2 * I;
+    rp.r0 = a.w13 + (erow + i) * rowb;
+    rp.r1 = a.w13 + (erow + I + i) * rowb;
+    rp.two = 1;
+    rp.issue(0, nch, lane);
+    float g, up;
+    rp.finish(xs, nch, lane, g, up);
+    if (lane == 0) ll_store(a.ll_act + p, silu_f(g) * up, epoch);
+  }
 
+  {
     // ---- phase 4: all activations, this CTA's W2 rows, out slice
-    const bool ok = ll_gather(a.ll_act, acts, P + Is, tid, kDecThreads, epoch, global_ns() + a.timeout_ns);
+    // One thread per CTA counts CTAs in and waits for all G of them; only then
+    // do all threads read the exchange words (one pass when they have landed;
+    // the epoch tags still catch any word not yet visible).  Polling the words
+    // themselves from every thread of every CTA congests the L2 lines they
+    // live in and delays the producers' stores.
+    __syncthreads();
+    bool ok = true;
+    if (tid == 0 && !s_fail) {
+      uint32_t* cnt = &a.ctrl->arrive[epoch & 1u];
+      atomicAdd(cnt, 1u);
+      const uint64_t deadline = global_ns() + a.timeout_ns;
+      while (ld_relaxed_u32(cnt) < static_cast<uint32_t>(G)) {
+        if (global_ns() > deadline) { ok = false; break; }
+      }
+      if (!ok) s_fail = kDevTimeoutAct;
+    }
+    __syncthreads();
+    if (!s_fail) ok = ll_gather(a.ll_act, acts, P + Is, tid, kDecThreads, epoch, global_ns() + a.timeout_ns);
     if (!ok) s_fail = kDevTimeoutAct;
     if (tid == 0 && !mbar_wait_until(&bar, 0, global_ns() + a.timeout_ns)) s_fail = kDevTimeoutCopy;
     __syncthreads();
     if (!s_fail) {
-      // Teams of 16 threads, one output row per team; each thread covers a
-      // 1/16 slice of every expert's row with independent partial sums, so
-      // the k+1 short dot products run in parallel instead of one after another.
-      // A warp holds two teams (rows rbase, rbase + 1); the loop bound is
-      // warp-uniform so every lane reaches the shuffles.
+      // Fold the routing weight (and the shared gate) into the activations,
+      // so each output is one dot product over the concatenated
+      // [k*I routed | Is shared] activation vector.  Integer quotients come
+      // from an fp32 reciprocal, exact for indices below 2^22.
+      const float inv_I = 1.0f / static_cast<float>(I);
+      for (int i = tid; i < P + Is; i += kDecThreads) {
+        const int j = i < P ? __float2int_rz((static_cast<float>(i) + 0.5f) * inv_I) : k;
+        acts[i] *= j < k ? s_w[j] : s_gate;
+      }
+      __syncthreads();
+      // Two output rows per warp, 16 threads per row; thread tl takes chunks
+      // tl, tl+16, ... (16-byte chunks of 8 weights) into four independent
+      // accumulators.  The loop bound is warp-uniform so every lane reaches the
+      // shuffles.
+      const int cpe = I >> 3;
+      const int nchunk = (P + Is) >> 3;
+      const float inv_cpe = 1.0f / static_cast<float>(cpe);
       const int tl = tid & 15;
       for (int rbase = warp * 2; rbase < hn; rbase += kDecThreads / 16) {
         const int r = rbase + ((tid >> 4) & 1);
         const bool active = r < hn;
-        float acc = 0.f;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
         if (active) {
-#pragma unroll 4
-          for (int j = 0; j < k; ++j) {
-            const uint8_t* row = w2s + (static_cast<size_t>(j) * hn + r) * I * 2;
-            acc = fmaf(s_w[j], smem_row_dot16<DT>(row, acts + static_cast<size_t>(j) * I, I, tl), acc);
-          }
-          if (Is > 0) {
-            const uint8_t* row = w2s + (static_cast<size_t>(k) * hn * I + static_cast<size_t>(r) * Is) * 2;
-            acc = fmaf(s_gate, smem_row_dot16<DT>(row, acts + P, Is, tl), acc);
+          const uint8_t* rrow = w2s + static_cast<size_t>(r) * I * 2;
+          const uint8_t* srow = w2s + (static_cast<size_t>(k) * hn * I + static_cast<size_t>(r) * Is) * 2;
+          for (int c0 = tl; c0 < nchunk; c0 += 64) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int c = c0 + 16 * u;
+              if (c < nchunk) {
+                const int j = __float2int_rz((static_cast<float>(c) + 0.5f) * inv_cpe);
+                const uint8_t* wp = j < k ? rrow + (static_cast<size_t>(j) * hn * I + (c - j * cpe) * 8) * 2
+                                          : srow + static_cast<size_t>(c - k * cpe) * 16;
+                const uint4 v = *reinterpret_cast<const uint4*>(wp);
+                const float4 xa = reinterpret_cast<const float4*>(acts)[2 * c];
+                const float4 xb = reinterpret_cast<const float4*>(acts)[2 * c + 1];
+                float f[8];
+                unpack8<DT>(v, f);
+                float t = f[0] * xa.x;
+                t = fmaf(f[1], xa.y, t); t = fmaf(f[2], xa.z, t); t = fmaf(f[3], xa.w, t);
+                t = fmaf(f[4], xb.x, t); t = fmaf(f[5], xb.y, t); t = fmaf(f[6], xb.z, t);
+                t = fmaf(f[7], xb.w, t);
+                acc[u] += t;
+              }
+            }
           }
         }
+        float sum = (acc[0] + acc[1]) + (acc[2] + acc[3]);
 #pragma unroll
-        for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (active && tl == 0) store_out(a.out, h0 + r, acc, a.out_dtype);
+        for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        if (active && tl == 0) store_out(a.out, h0 + r, sum, a.out_dtype);
       }
       // Every CTA has read the epoch before publishing its activations and CTA 0
       // has now seen all of them, so the next launch may use the next epoch.
@@ -392,6 +455,7 @@ moe_status_t launch_decode_fused(const moe_cfg_t& c, const BlockPtrs& p, uint8_t
   a.ll_act = reinterpret_cast<uint64_t*>(ws + L.ll_act);
   a.H = c.hidden; a.E = c.n_experts; a.k = c.top_k; a.I = c.inter; a.Is = c.shared_inter;
   a.has_gate = c.has_shared_gate; a.norm_topk = c.norm_topk; a.out_dtype = c.out_dtype;
+  a.static_weights = (c.flags & MOE_FLAG_STATIC_WEIGHTS) ? 1 : 0;
   size_t smem;
   decode_smem_layout(c, G, a.off_lg, a.off_act, a.off_w2, smem);
   a.timeout_ns = wait_timeout_ns();

@@ -44,10 +44,16 @@ __global__ void __launch_bounds__(1024) group_kernel(const int32_t* __restrict__
   for (int e = tid; e < n; e += 1024) cnt[e] = 0;
   __syncthreads();
   const int np = T * k;
-  for (int p = tid; p < np; p += 1024) {
-    const int e = ids[p];
-    if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
-    else report_error(ctrl, kDevBadExpert, static_cast<uint32_t>(p));
+  for (int base = tid; base < np; base += 1024 * 8) {  // 8 id loads in flight per thread
+    int ev[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) ev[u] = base + 1024 * u < np ? ids[base + 1024 * u] : -2;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int e = ev[u];
+      if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+      else if (e != -2) report_error(ctrl, kDevBadExpert, static_cast<uint32_t>(base + 1024 * u));
+    }
   }
   if (tid == 0) cnt[E] = has_shared ? T : 0;
   __syncthreads();
@@ -109,9 +115,15 @@ __global__ void __launch_bounds__(1024) group_kernel(const int32_t* __restrict__
   }
   __syncthreads();
   // File routed pairs (any order within an expert) and the shared pairs (in token order).
-  for (int p = tid; p < np; p += 1024) {
-    const int e = ids[p];
-    if (e >= 0 && e < E) perm[atomicAdd(&cur[e], 1)] = p;
+  for (int base = tid; base < np; base += 1024 * 8) {
+    int ev[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) ev[u] = base + 1024 * u < np ? ids[base + 1024 * u] : -2;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int e = ev[u];
+      if (e >= 0 && e < E) perm[atomicAdd(&cur[e], 1)] = base + 1024 * u;
+    }
   }
   if (has_shared)
     for (int t = tid; t < T; t += 1024) perm[cur[E] + t] = np + t;
@@ -256,13 +268,28 @@ __global__ void __launch_bounds__(kGThreads) grouped_w2_kernel(
 // ---------------------------------------------------------------- combine
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, int T, int H, int k,
                                                       int has_shared, void* out, int out_dtype) {
-  const size_t n = static_cast<size_t>(T) * H;
-  for (size_t idx = blockIdx.x * 256ull + threadIdx.x; idx < n; idx += static_cast<size_t>(gridDim.x) * 256) {
-    const size_t t = idx / H, h = idx - t * H;
-    float acc = 0.f;
-    for (int j = 0; j < k; ++j) acc += y[(t * k + j) * H + h];
-    if (has_shared) acc += y[(static_cast<size_t>(T) * k + t) * H + h];
-    store_out(out, idx, acc, out_dtype);
+  // four consecutive outputs per thread (H % 8 == 0), the k (+1) slot loads
+  // issued ahead of the adds; the sum runs in slot order, then the shared part
+  const int H4 = H >> 2;
+  const size_t n4 = static_cast<size_t>(T) * H4;
+  const float4* y4 = reinterpret_cast<const float4*>(y);
+  for (size_t idx = blockIdx.x * 256ull + threadIdx.x; idx < n4; idx += static_cast<size_t>(gridDim.x) * 256) {
+    const size_t t = idx / H4, h4 = idx - t * H4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+    for (int j = 0; j < k; ++j) {
+      const float4 v = y4[(t * k + j) * H4 + h4];
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    if (has_shared) {
+      const float4 v = y4[(static_cast<size_t>(T) * k + t) * H4 + h4];
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    const size_t o = t * H + 4 * h4;
+    store_out(out, o, acc.x, out_dtype);
+    store_out(out, o + 1, acc.y, out_dtype);
+    store_out(out, o + 2, acc.z, out_dtype);
+    store_out(out, o + 3, acc.w, out_dtype);
   }
 }
 
@@ -330,7 +357,7 @@ moe_status_t launch_grouped(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws,
     }
     if (moe_status_t s = check_launch("grouped_w2_kernel")) return s;
   }
-  const long long n = static_cast<long long>(T) * H;
+  const long long n = static_cast<long long>(T) * (H / 4);
   const int gc = static_cast<int>((n + 255) / 256 < sms * 16LL ? (n + 255) / 256 : sms * 16LL);
   combine_kernel<<<gc, 256, 0, st>>>(y, T, H, k, Is > 0, p.out, c.out_dtype);
   if (moe_status_t s = check_launch("combine_kernel")) return s;

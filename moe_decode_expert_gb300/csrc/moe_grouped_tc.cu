@@ -683,12 +683,24 @@ __global__ void __launch_bounds__(256) tc_gather_kernel(const uint8_t* __restric
                                                         int P, int T, int k, int H, uint8_t* __restrict__ xs) {
   const int nch = H >> 3;
   const size_t total = static_cast<size_t>(P) * nch;
-  for (size_t i = blockIdx.x * 256ull + threadIdx.x; i < total; i += static_cast<size_t>(gridDim.x) * 256) {
-    const int pos = static_cast<int>(i / nch), c = static_cast<int>(i - static_cast<size_t>(pos) * nch);
-    const int p = perm[pos];
-    const int t = p < T * k ? p / k : p - T * k;
-    const uint4 v = ld_nc16(x + (static_cast<size_t>(t) * H + 8 * c) * 2);
-    *reinterpret_cast<uint4*>(xs + (static_cast<size_t>(pos) * H + 8 * c) * 2) = v;
+  const size_t stride = static_cast<size_t>(gridDim.x) * 256;
+  for (size_t base = blockIdx.x * 256ull + threadIdx.x; base < total; base += stride * 4) {
+    uint4 v[4];
+    size_t dst[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {  // 4 row chunks in flight per thread
+      const size_t i = base + stride * u;
+      if (i < total) {
+        const int pos = static_cast<int>(i / nch), c = static_cast<int>(i - static_cast<size_t>(pos) * nch);
+        const int p = perm[pos];
+        const int t = p < T * k ? p / k : p - T * k;
+        v[u] = ld_nc16(x + (static_cast<size_t>(t) * H + 8 * c) * 2);
+        dst[u] = (static_cast<size_t>(pos) * H + 8 * c) * 2;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (base + stride * u < total) *reinterpret_cast<uint4*>(xs + dst[u]) = v[u];
   }
 }
 

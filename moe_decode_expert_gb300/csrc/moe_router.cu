@@ -101,13 +101,29 @@ __global__ void __launch_bounds__(256) router_gemv_kernel(const uint8_t* __restr
     const int kw = min(2048, H - k0);
     const int nch = kw >> 3;
     __syncthreads();
-    for (int idx = threadIdx.x; idx < nt * nch; idx += 256) {
-      const int t = idx / nch, c = idx - t * nch;
-      float f[8];
-      unpack8<DT>(ld_nc16(x + (static_cast<size_t>(t0 + t) * H + k0 + 8 * c) * 2), f);
-      float4* d = reinterpret_cast<float4*>(xt + static_cast<size_t>(t) * 2048 + 8 * c);
-      d[0] = make_float4(f[0], f[1], f[2], f[3]);
-      d[1] = make_float4(f[4], f[5], f[6], f[7]);
+    // 8 loads in flight per thread before any is used (the tile is up to 16 x 2048).
+    for (int base = threadIdx.x; base < nt * nch; base += 256 * 8) {
+      uint4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int idx = base + 256 * u;
+        if (idx < nt * nch) {
+          const int t = idx / nch, c = idx - t * nch;
+          v[u] = ld_nc16(x + (static_cast<size_t>(t0 + t) * H + k0 + 8 * c) * 2);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int idx = base + 256 * u;
+        if (idx < nt * nch) {
+          const int t = idx / nch, c = idx - t * nch;
+          float f[8];
+          unpack8<DT>(v[u], f);
+          float4* d = reinterpret_cast<float4*>(xt + static_cast<size_t>(t) * 2048 + 8 * c);
+          d[0] = make_float4(f[0], f[1], f[2], f[3]);
+          d[1] = make_float4(f[4], f[5], f[6], f[7]);
+        }
+      }
     }
     __syncthreads();
     if (row) {

@@ -27,8 +27,8 @@ def _to(d, dev=DEV):
     return {k: (v.to(dev) if v is not None else None) for k, v in d.items()}
 
 
-def _decode(m, wl, g, out_dtype=None, ws=None):
-    cfg = m.cfg_from_workload(wl, out_dtype)
+def _decode(m, wl, g, out_dtype=None, ws=None, flags=0):
+    cfg = m.cfg_from_workload(wl, out_dtype, flags)
     ids = torch.full((1, wl.top_k), -1, dtype=torch.int32, device=DEV)
     w = torch.full((1, wl.top_k), float("nan"), dtype=torch.float32, device=DEV)
     out = torch.full((1, wl.hidden), float("nan"), dtype=cfg.out_torch_dtype, device=DEV)
@@ -71,13 +71,14 @@ def test_tiny_config(m, out_dtype):
             assert np.all(np.abs(got - ref16) <= ulp + 1e-12)
 
 
+@pytest.mark.parametrize("flags", [0, 4], ids=["plain", "static_weights"])
 @pytest.mark.parametrize("name", ["sharded_decode", "full_decode"])
-def test_full_size_layers(m, name):
+def test_full_size_layers(m, name, flags):
     wl = moe_synth.workload(name)
     ws = m.alloc_workspace(m.cfg_from_workload(wl), 1, DEV)
     for layer in (0, 17, 35):
         g = moe_synth.make_layer(wl, layer, 1, device=DEV)
-        ids, w, out = _decode(m, wl, g, ws=ws)
+        ids, w, out = _decode(m, wl, g, ws=ws, flags=flags)
         ref = oracle_sampled(wl, g, [0])
         assert min_rank_gap(ref["logits"], wl.top_k)[0] > 1e-4
         assert np.array_equal(ids.cpu().numpy(), ref["ids"])
@@ -201,10 +202,11 @@ def test_repeated_calls_share_one_workspace(m):
         parity(out, r["out"])
 
 
-def test_cuda_graph_of_layers(m):
-    """36 rotated layers captured in one CUDA graph and replayed: equal to eager."""
+@pytest.mark.parametrize("flags", [0, 4], ids=["plain", "static_weights"])
+def test_cuda_graph_of_layers(m, flags):
+    """Rotated layers captured in one CUDA graph and replayed: equal to eager."""
     wl = moe_synth.workload("sharded_decode")
-    cfg = m.cfg_from_workload(wl)
+    cfg = m.cfg_from_workload(wl, None, flags)
     L = 4
     layers = [moe_synth.make_layer(wl, l, 1, device=DEV) for l in range(L)]
     ws = m.alloc_workspace(cfg, 1, DEV)
@@ -218,6 +220,7 @@ def test_cuda_graph_of_layers(m):
                                  g["shared_gate_w"], ids[l], ws_[l], outs[l], ws)
 
     s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())  # the layers were generated on the default stream
     with torch.cuda.stream(s):
         step()
     torch.cuda.synchronize()
