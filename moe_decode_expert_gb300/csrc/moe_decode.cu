@@ -110,8 +110,11 @@ struct RowPair {
   }
 };
 
-template <int DT>
-__global__ void __launch_bounds__(kDecThreads, 2) decode_fused_kernel(const DecodeArgs a) {
+// DEPTH 1: one gate/up pair in flight per warp (<= 128 registers, two CTAs per
+// SM fit); DEPTH 2: two pairs in flight (one CTA per SM), for configs with more
+// routed pairs per CTA than warps.
+template <int DT, int DEPTH>
+__global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(const DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t bar;
   __shared__ int s_ids[32];
@@ -256,32 +259,55 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_fused_kernel(const Deco
   }
 
   // ---- phase 3: this CTA's share of the k*I routed gate/up pairs; a warp
-  // starts a pair as soon as the pair's expert has been ranked.
+  // starts a pair as soon as the pair's expert has been ranked.  With
+  // DEPTH == 2 a warp keeps two pairs' rows in flight at once.
   const int P = k * I;
-  for (int qq = warp;; qq += kDecWarps) {
-    const int p = qq * G + cta;
-    if (p >= P) break;
-    const int j = p / I, i = p - j * I;
+  auto wait_slot = [&](int j) -> bool {
     const uint64_t deadline = global_ns() + a.timeout_ns;
-    bool ready = true;
     while (s_ready[j] == 0) {
-      if (global_ns() > deadline) { ready = false; break; }
+      if (global_ns() > deadline) return false;
       __nanosleep(32);
     }
     __threadfence_block();
-    if (!ready) {
+    return true;
+  };
+  auto start_pair = [&](RowPair<DT>& r, int p) -> bool {
+    const int j = p / I, i = p - j * I;
+    if (!wait_slot(j)) {
       if (lane == 0) s_fail = kDevTimeoutLogits;
-      break;
+      return false;
     }
-    if (s_fail) break;
+    if (s_fail) return false;
     const size_t erow = static_cast<size_t>(s_ids[j]) * 2 * I;
-    rp.r0 = a.w13 + (erow + i) * rowb;
-    rp.r1 = a.w13 + (erow + I + i) * rowb;
-    rp.two = 1;
-    rp.issue(0, nch, lane);
+    r.r0 = a.w13 + (erow + i) * rowb;
+    r.r1 = a.w13 + (erow + I + i) * rowb;
+    r.two = 1;
+    r.issue(0, nch, lane);
+    return true;
+  };
+  auto end_pair = [&](RowPair<DT>& r, int p) {
     float g, up;
-    rp.finish(xs, nch, lane, g, up);
+    r.finish(xs, nch, lane, g, up);
     if (lane == 0) ll_store(a.ll_act + p, silu_f(g) * up, epoch);
+  };
+  if constexpr (DEPTH == 2) {
+    RowPair<DT> rq;
+    for (int qq = warp;; qq += 2 * kDecWarps) {
+      const int pa = qq * G + cta, pb = (qq + kDecWarps) * G + cta;
+      if (pa >= P) break;
+      if (!start_pair(rp, pa)) break;
+      const bool has_b = pb < P && start_pair(rq, pb);
+      end_pair(rp, pa);
+      if (!has_b) break;
+      end_pair(rq, pb);
+    }
+  } else {
+    for (int qq = warp;; qq += kDecWarps) {
+      const int p = qq * G + cta;
+      if (p >= P) break;
+      if (!start_pair(rp, p)) break;
+      end_pair(rp, p);
+    }
   }
 
   {
@@ -407,14 +433,14 @@ size_t decode_smem_bytes(const moe_cfg_t& c, int G) {
   return t;
 }
 
-template <int DT>
+template <int DT, int DEPTH>
 static moe_status_t launch_decode_dt(const DecodeArgs& args, int G, size_t smem, cudaStream_t st) {
   static int configured_dev = -1;
   static size_t configured_smem = 0;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_dev != dev || configured_smem < smem) {
-    if (cudaFuncSetAttribute(decode_fused_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(decode_fused_kernel<DT, DEPTH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return check_launch("cudaFuncSetAttribute(decode)");
     configured_dev = dev;
@@ -430,7 +456,7 @@ static moe_status_t launch_decode_dt(const DecodeArgs& args, int G, size_t smem,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, decode_fused_kernel<DT>, args) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, decode_fused_kernel<DT, DEPTH>, args) != cudaSuccess)
     return check_launch("decode_fused_kernel");
   stat_kernels(1);
   return MOE_OK;
@@ -461,8 +487,11 @@ moe_status_t launch_decode_fused(const moe_cfg_t& c, const BlockPtrs& p, uint8_t
   a.timeout_ns = wait_timeout_ns();
   if (smem > 227 * 1024)
     return set_error(MOE_ERR_UNSUPPORTED, "decode: needs %zu B of shared memory per CTA (max 232448)", smem);
-  if (c.dtype == MOE_BF16) return launch_decode_dt<MOE_BF16>(a, G, smem, st);
-  return launch_decode_dt<MOE_F16>(a, G, smem, st);
+  // two pairs in flight per warp when a CTA has more routed pairs than warps
+  const bool deep = (c.top_k * c.inter + G - 1) / G > kDecWarps;
+  if (c.dtype == MOE_BF16)
+    return deep ? launch_decode_dt<MOE_BF16, 2>(a, G, smem, st) : launch_decode_dt<MOE_BF16, 1>(a, G, smem, st);
+  return deep ? launch_decode_dt<MOE_F16, 2>(a, G, smem, st) : launch_decode_dt<MOE_F16, 1>(a, G, smem, st);
 }
 
 }  // namespace moe
