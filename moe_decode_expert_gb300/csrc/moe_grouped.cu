@@ -268,29 +268,34 @@ __global__ void __launch_bounds__(kGThreads) grouped_w2_kernel(
 // ---------------------------------------------------------------- combine
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, int T, int H, int k,
                                                       int has_shared, void* out, int out_dtype) {
-  // four consecutive outputs per thread (H % 8 == 0), the k (+1) slot loads
-  // issued ahead of the adds; the sum runs in slot order, then the shared part
+  // grid (ceil(H/4 / 256), T): four consecutive outputs of token blockIdx.y per
+  // thread (H % 8 == 0); the sum runs in slot order, then the shared part
   const int H4 = H >> 2;
-  const size_t n4 = static_cast<size_t>(T) * H4;
+  const int h4 = blockIdx.x * 256 + threadIdx.x;
+  const int t = blockIdx.y;
+  if (h4 >= H4 || t >= T) return;
   const float4* y4 = reinterpret_cast<const float4*>(y);
-  for (size_t idx = blockIdx.x * 256ull + threadIdx.x; idx < n4; idx += static_cast<size_t>(gridDim.x) * 256) {
-    const size_t t = idx / H4, h4 = idx - t * H4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-    for (int j = 0; j < k; ++j) {
-      const float4 v = y4[(t * k + j) * H4 + h4];
-      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+  const int nk = k + (has_shared ? 1 : 0);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j0 = 0; j0 < nk; j0 += 8) {  // eight slot loads in flight, then add in order
+    float4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int j = j0 + u;
+      if (j < nk) {
+        const size_t row = j < k ? static_cast<size_t>(t) * k + j : static_cast<size_t>(T) * k + t;
+        v[u] = y4[row * H4 + h4];
+      }
     }
-    if (has_shared) {
-      const float4 v = y4[(static_cast<size_t>(T) * k + t) * H4 + h4];
-      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-    }
-    const size_t o = t * H + 4 * h4;
-    store_out(out, o, acc.x, out_dtype);
-    store_out(out, o + 1, acc.y, out_dtype);
-    store_out(out, o + 2, acc.z, out_dtype);
-    store_out(out, o + 3, acc.w, out_dtype);
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (j0 + u < nk) { acc.x += v[u].x; acc.y += v[u].y; acc.z += v[u].z; acc.w += v[u].w; }
   }
+  const size_t o = static_cast<size_t>(t) * H + 4 * h4;
+  store_out(out, o, acc.x, out_dtype);
+  store_out(out, o + 1, acc.y, out_dtype);
+  store_out(out, o + 2, acc.z, out_dtype);
+  store_out(out, o + 3, acc.w, out_dtype);
 }
 
 moe_status_t launch_grouped(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws, const WsLayout& L,
@@ -357,9 +362,7 @@ moe_status_t launch_grouped(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws,
     }
     if (moe_status_t s = check_launch("grouped_w2_kernel")) return s;
   }
-  const long long n = static_cast<long long>(T) * (H / 4);
-  const int gc = static_cast<int>((n + 255) / 256 < sms * 16LL ? (n + 255) / 256 : sms * 16LL);
-  combine_kernel<<<gc, 256, 0, st>>>(y, T, H, k, Is > 0, p.out, c.out_dtype);
+  combine_kernel<<<dim3((H / 4 + 255) / 256, T), 256, 0, st>>>(y, T, H, k, Is > 0, p.out, c.out_dtype);
   if (moe_status_t s = check_launch("combine_kernel")) return s;
   stat_kernels(4);
   return MOE_OK;

@@ -36,7 +36,7 @@ namespace moe {
 constexpr int kTcThreads = 192;
 constexpr int kBK = 64;                 // K elements per stage: one 128-byte swizzle row
 constexpr uint32_t kTileA = 128 * 128;  // 128 rows x 128 bytes
-constexpr int kSmemBudget = 196 * 1024;
+constexpr int kSmemBudget = 220 * 1024;
 
 struct TcTile {
   int32_t e;     // expert id, E = shared expert
@@ -150,14 +150,20 @@ __device__ __forceinline__ bool epi_any(bool v) {
 }
 
 // ======================================================= W13 + SiLU pass
-template <int DT, int N>
+// MT 128-row M-tiles (each 64 gate rows stacked on the matching 64 up rows) of
+// one expert share every token (B) stage, so the token operand is read from L2
+// once per MT M-tiles; each tile has its own TMEM accumulator (2*MT*N columns
+// with double buffering).
+template <int DT, int N, int MT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_w13_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapAs,
                   const __grid_constant__ CUtensorMap mapB, const TcTile* __restrict__ tiles,
                   const int32_t* __restrict__ n_tiles_p, int H, int I, int Is, int E, int act_stride,
                   uint16_t* __restrict__ act_hi, uint16_t* __restrict__ act_lo, Control* ctrl, uint64_t timeout) {
-  constexpr uint32_t kStage = kTileA + N * 128;
-  constexpr int kStages = (kSmemBudget - 128 * 17 * 4) / kStage > 8 ? 8 : (kSmemBudget - 128 * 17 * 4) / kStage;
+  constexpr uint32_t kStage = MT * kTileA + N * 128;
+  constexpr int kStg = 128 * 17 * 4;
+  constexpr int kStages = (kSmemBudget - kStg) / kStage > 8 ? 8 : (kSmemBudget - kStg) / kStage;
+  constexpr uint32_t kCols = 2 * MT * N;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* stg = reinterpret_cast<float*>(smem + kStages * kStage);  // [128][17] epilogue staging
@@ -174,7 +180,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     s_abort = 0;
   }
   if (warp == 1) {
-    tmem_alloc(&tmem_base_s, 2 * N);
+    tmem_alloc(&tmem_base_s, kCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -194,7 +200,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const bool sh = tl.e == E;
         const CUtensorMap* mA = sh ? &mapAs : &mapA;
         const int ie = sh ? Is : I;
-        const int rowg = (sh ? 0 : tl.e * 2 * I) + tl.m * 64;
+        const int m0 = tl.m * MT;
+        const int nv = min(MT, ie / 64 - m0);
+        const int rowg = (sh ? 0 : tl.e * 2 * I) + m0 * 64;
+        const uint32_t bytes = static_cast<uint32_t>(nv) * kTileA + N * 128;
         for (int kb = 0; kb < KB; ++kb) {
           if (!tc_wait(&empty[stage], phase ^ 1u, timeout, &s_abort)) {
             s_abort = 1;
@@ -202,10 +211,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             break;
           }
           uint8_t* sA = smem + stage * kStage;
-          mbar_arrive_expect_tx(&full[stage], kStage);
-          tma_load_2d(sA, mA, &full[stage], kb * kBK, rowg);
-          tma_load_2d(sA + kTileA / 2, mA, &full[stage], kb * kBK, rowg + ie);
-          tma_load_2d(sA + kTileA, &mapB, &full[stage], kb * kBK, tl.pos0);
+          mbar_arrive_expect_tx(&full[stage], bytes);
+          for (int mt = 0; mt < nv; ++mt) {
+            tma_load_2d(sA + mt * kTileA, mA, &full[stage], kb * kBK, rowg + mt * 64);
+            tma_load_2d(sA + mt * kTileA + kTileA / 2, mA, &full[stage], kb * kBK, rowg + mt * 64 + ie);
+          }
+          tma_load_2d(sA + MT * kTileA, &mapB, &full[stage], kb * kBK, tl.pos0);
           issued_mask |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -222,6 +233,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       uint32_t phase = 0;
       int it = 0;
       for (int t = blockIdx.x; t < ntiles && !s_abort; t += gridDim.x, ++it) {
+        const TcTile tl = tiles[t];
+        const int ie = tl.e == E ? Is : I;
+        const int nv = min(MT, ie / 64 - tl.m * MT);
         const int acc = it & 1;
         if (!tc_wait(&tempty[acc], ((it >> 1) & 1) ^ 1u, timeout, &s_abort)) {
           s_abort = 1;
@@ -229,7 +243,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d = tbase + static_cast<uint32_t>(acc * N);
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb) {
           if (!tc_wait(&full[stage], phase, timeout, &s_abort)) {
@@ -238,10 +251,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           tc_fence_after();
           const uint32_t sA = smem_u32(smem + stage * kStage);
-          const uint32_t sB = sA + kTileA;
+          const uint32_t sB = sA + MT * kTileA;
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)
-            tc_mma(d, sw128_desc(sA + 32 * k), sw128_desc(sB + 32 * k), idesc, (kb | k) != 0);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+              if (mt < nv)
+                tc_mma(tbase + static_cast<uint32_t>((acc * MT + mt) * N), sw128_desc(sA + mt * kTileA + 32 * k),
+                       sw128_desc(sB + 32 * k), idesc, (kb | k) != 0);
           tc_commit(&empty[stage]);
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
@@ -257,10 +274,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else {  // ---------------------------------------------------- epilogue, 128 threads
     const int q = warp & 3;
-    const int row = 32 * q + lane;
+    const int row = 32 * q + lane;          // TMEM lane this thread reads
+    const int etid = threadIdx.x - 64;      // 0..127
+    const int ar = etid & 63, half = etid >> 6;  // activation row and column half it computes
     int it = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
       const TcTile tl = tiles[t];
+      const int ie = tl.e == E ? Is : I;
+      const int nv = min(MT, ie / 64 - tl.m * MT);
       const int acc = it & 1;
       const bool ok = !s_abort && tc_wait(&tfull[acc], (it >> 1) & 1, timeout, &s_abort);
       if (epi_any(!ok)) {
@@ -269,24 +290,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         break;
       }
       tc_fence_after();
-      for (int c0 = 0; c0 < tl.n; c0 += 16) {
-        float v[16];
-        tmem_ld16(tbase + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(acc * N + c0), v);
+      for (int mt = 0; mt < nv; ++mt) {
+        const int i = (tl.m * MT + mt) * 64 + ar;
+        for (int c0 = 0; c0 < tl.n; c0 += 16) {
+          float v[16];
+          tmem_ld16(tbase + (static_cast<uint32_t>(32 * q) << 16) +
+                        static_cast<uint32_t>((acc * MT + mt) * N + c0), v);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) stg[row * 17 + j] = v[j];
-        named_bar_sync(1, 128);
-        if (row < 64) {
-          const int i = tl.m * 64 + row;
+          for (int j = 0; j < 16; ++j) stg[row * 17 + j] = v[j];
+          named_bar_sync(1, 128);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
+          for (int jj = 0; jj < 8; ++jj) {
+            const int j = half * 8 + jj;
             const int col = c0 + j;
             if (col < tl.n) {
-              const float g = stg[row * 17 + j], u = stg[(row + 64) * 17 + j];
+              const float g = stg[ar * 17 + j], u = stg[(ar + 64) * 17 + j];
               split_store<DT>(act_hi, act_lo, static_cast<size_t>(tl.pos0 + col) * act_stride + i, silu_f(g) * u);
             }
           }
+          named_bar_sync(1, 128);
         }
-        named_bar_sync(1, 128);
       }
       tc_fence_before();
       __syncwarp();
@@ -297,12 +320,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tbase, 2 * N);
+    tmem_dealloc(tbase, kCols);
   }
 }
 
 // =========================================================== W2 pass
-template <int DT, int N>
+// MT 128-row M-tiles of W2 (output rows h) of one expert share every
+// activation (hi, lo) stage.
+template <int DT, int N, int MT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_w2_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapAs,
                  const __grid_constant__ CUtensorMap mapHi, const __grid_constant__ CUtensorMap mapLo,
@@ -311,8 +336,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                  const int32_t* __restrict__ perm, const float* __restrict__ topk_w,
                  const float* __restrict__ gate_logits, int gate_stride, int has_gate, int T, int H, int I, int Is,
                  int E, int k, float* __restrict__ y, Control* ctrl, uint64_t timeout) {
-  constexpr uint32_t kStage = kTileA + 2 * N * 128;
+  constexpr uint32_t kStage = MT * kTileA + 2 * N * 128;
   constexpr int kStages = kSmemBudget / kStage > 8 ? 8 : kSmemBudget / kStage;
+  constexpr uint32_t kCols = 2 * MT * N;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t full[kStages], empty[kStages], tfull[2], tempty[2], done;
@@ -330,7 +356,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     s_abort = 0;
   }
   if (warp == 1) {
-    tmem_alloc(&tmem_base_s, 2 * N);
+    tmem_alloc(&tmem_base_s, kCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -338,6 +364,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_after();
   const uint32_t tbase = tmem_base_s;
   const int ntiles = *n_tiles_p;
+  const int mtiles = H / 128;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -351,7 +378,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const CUtensorMap* mH = sh ? &mapHiS : &mapHi;
         const CUtensorMap* mL = sh ? &mapLoS : &mapLo;
         const int KB = (sh ? Is : I) / kBK;
-        const int rowa = (sh ? 0 : tl.e * H) + tl.m * 128;
+        const int m0 = tl.m * MT;
+        const int nv = min(MT, mtiles - m0);
+        const int rowa = (sh ? 0 : tl.e * H) + m0 * 128;
+        const uint32_t bytes = static_cast<uint32_t>(nv) * kTileA + 2 * N * 128;
         for (int kb = 0; kb < KB; ++kb) {
           if (!tc_wait(&empty[stage], phase ^ 1u, timeout, &s_abort)) {
             s_abort = 1;
@@ -359,10 +389,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             break;
           }
           uint8_t* sA = smem + stage * kStage;
-          mbar_arrive_expect_tx(&full[stage], kStage);
-          tma_load_2d(sA, mA, &full[stage], kb * kBK, rowa);
-          tma_load_2d(sA + kTileA, mH, &full[stage], kb * kBK, tl.pos0);
-          tma_load_2d(sA + kTileA + N * 128, mL, &full[stage], kb * kBK, tl.pos0);
+          mbar_arrive_expect_tx(&full[stage], bytes);
+          for (int mt = 0; mt < nv; ++mt) tma_load_2d(sA + mt * kTileA, mA, &full[stage], kb * kBK, rowa + mt * 128);
+          tma_load_2d(sA + MT * kTileA, mH, &full[stage], kb * kBK, tl.pos0);
+          tma_load_2d(sA + MT * kTileA + N * 128, mL, &full[stage], kb * kBK, tl.pos0);
           issued_mask |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -380,6 +410,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int t = blockIdx.x; t < ntiles && !s_abort; t += gridDim.x, ++it) {
         const TcTile tl = tiles[t];
         const int KB = (tl.e == E ? Is : I) / kBK;
+        const int nv = min(MT, mtiles - tl.m * MT);
         const int acc = it & 1;
         if (!tc_wait(&tempty[acc], ((it >> 1) & 1) ^ 1u, timeout, &s_abort)) {
           s_abort = 1;
@@ -387,7 +418,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d = tbase + static_cast<uint32_t>(acc * N);
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb) {
           if (!tc_wait(&full[stage], phase, timeout, &s_abort)) {
@@ -396,12 +426,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           tc_fence_after();
           const uint32_t sA = smem_u32(smem + stage * kStage);
-          const uint32_t sH = sA + kTileA, sL = sH + N * 128;
+          const uint32_t sH = sA + MT * kTileA, sL = sH + N * 128;
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            tc_mma(d, sw128_desc(sA + 32 * kk), sw128_desc(sH + 32 * kk), idesc, (kb | kk) != 0);
-            tc_mma(d, sw128_desc(sA + 32 * kk), sw128_desc(sL + 32 * kk), idesc, 1u);
-          }
+          for (int kk = 0; kk < kBK / 16; ++kk)
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+              if (mt < nv) {
+                const uint32_t d = tbase + static_cast<uint32_t>((acc * MT + mt) * N);
+                tc_mma(d, sw128_desc(sA + mt * kTileA + 32 * kk), sw128_desc(sH + 32 * kk), idesc, (kb | kk) != 0);
+                tc_mma(d, sw128_desc(sA + mt * kTileA + 32 * kk), sw128_desc(sL + 32 * kk), idesc, 1u);
+              }
           tc_commit(&empty[stage]);
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
@@ -422,6 +456,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int it = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
       const TcTile tl = tiles[t];
+      const int nv = min(MT, mtiles - tl.m * MT);
       const int acc = it & 1;
       if (epi_any(s_abort != 0)) break;  // also: previous tile's readers of s_pair / s_wt are done
       for (int c = etid; c < tl.n; c += 128) {
@@ -439,14 +474,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         break;
       }
       tc_fence_after();
-      const int h = tl.m * 128 + row;
-      for (int c0 = 0; c0 < tl.n; c0 += 16) {
-        float v[16];
-        tmem_ld16(tbase + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(acc * N + c0), v);
+      for (int mt = 0; mt < nv; ++mt) {
+        const int h = (tl.m * MT + mt) * 128 + row;
+        for (int c0 = 0; c0 < tl.n; c0 += 16) {
+          float v[16];
+          tmem_ld16(tbase + (static_cast<uint32_t>(32 * q) << 16) +
+                        static_cast<uint32_t>((acc * MT + mt) * N + c0), v);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int col = c0 + j;
-          if (col < tl.n) y[static_cast<size_t>(s_pair[col]) * H + h] = s_wt[col] * v[j];
+          for (int j = 0; j < 16; ++j) {
+            const int col = c0 + j;
+            if (col < tl.n) y[static_cast<size_t>(s_pair[col]) * H + h] = s_wt[col] * v[j];
+          }
         }
       }
       tc_fence_before();
@@ -458,10 +496,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tbase, 2 * N);
+    tmem_dealloc(tbase, kCols);
   }
 }
-
 
 // ======================================================== router GEMM (large T)
 // logits[t, e] = x[t] . Wr[e] for T tokens on tcgen05: router rows are M (128
@@ -613,8 +650,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // Layout of `sched`: [0] n13, [1] n2, then TcTile arrays at the offsets given.
 __global__ void __launch_bounds__(1024) tc_schedule_kernel(const int32_t* __restrict__ counts,
                                                            const int32_t* __restrict__ offsets, int E, int I,
-                                                           int Is, int H, int N, int32_t* n13, int32_t* n2,
-                                                           TcTile* t13, TcTile* t2) {
+                                                           int Is, int H, int N, int mt13, int mt2, int32_t* n13,
+                                                           int32_t* n2, TcTile* t13, TcTile* t2) {
   __shared__ unsigned long long wtot[32];
   __shared__ int pre13[1026], pre2[1026];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -627,8 +664,8 @@ __global__ void __launch_bounds__(1024) tc_schedule_kernel(const int32_t* __rest
       const int cnt = counts[e];
       const int ie = e == E ? Is : I;
       const int nt = (cnt + N - 1) / N;
-      a13[s] = ie > 0 ? nt * (ie / 64) : 0;
-      a2[s] = ie > 0 ? nt * (H / 128) : 0;
+      a13[s] = ie > 0 ? nt * ((ie / 64 + mt13 - 1) / mt13) : 0;
+      a2[s] = ie > 0 ? nt * ((H / 128 + mt2 - 1) / mt2) : 0;
     }
   }
   unsigned long long v = (static_cast<unsigned long long>(a13[0] + a13[1]) << 32) | static_cast<unsigned>(a2[0] + a2[1]);
@@ -670,7 +707,7 @@ __global__ void __launch_bounds__(1024) tc_schedule_kernel(const int32_t* __rest
     }
     const int e = lo;
     const int ie = e == E ? Is : I;
-    const int per_n = second ? H / 128 : ie / 64;  // M-tiles per N-tile
+    const int per_n = second ? (H / 128 + mt2 - 1) / mt2 : (ie / 64 + mt13 - 1) / mt13;  // M-groups per N-tile
     const int j = (ii - pre[e]) / per_n, mm = (ii - pre[e]) - j * per_n;
     const int cnt = counts[e];
     const TcTile tl{e, mm, offsets[e] + j * N, min(N, cnt - j * N)};
@@ -678,29 +715,27 @@ __global__ void __launch_bounds__(1024) tc_schedule_kernel(const int32_t* __rest
   }
 }
 
-// Xs[pos, :] = x[token of perm[pos], :] (16-byte chunks).
+// Xs[pos, :] = x[token of perm[pos], :]: one warp per row, 16-byte chunks,
+// up to 8 chunks per lane in flight.
 __global__ void __launch_bounds__(256) tc_gather_kernel(const uint8_t* __restrict__ x, const int32_t* __restrict__ perm,
                                                         int P, int T, int k, int H, uint8_t* __restrict__ xs) {
+  const int lane = threadIdx.x & 31;
+  const int warps = gridDim.x * 8;
   const int nch = H >> 3;
-  const size_t total = static_cast<size_t>(P) * nch;
-  const size_t stride = static_cast<size_t>(gridDim.x) * 256;
-  for (size_t base = blockIdx.x * 256ull + threadIdx.x; base < total; base += stride * 4) {
-    uint4 v[4];
-    size_t dst[4];
+  for (int pos = blockIdx.x * 8 + (threadIdx.x >> 5); pos < P; pos += warps) {
+    const int p = perm[pos];
+    const int t = p < T * k ? p / k : p - T * k;
+    const uint8_t* src = x + static_cast<size_t>(t) * H * 2;
+    uint8_t* dst = xs + static_cast<size_t>(pos) * H * 2;
+    for (int c0 = lane; c0 < nch; c0 += 32 * 8) {
+      uint4 v[8];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {  // 4 row chunks in flight per thread
-      const size_t i = base + stride * u;
-      if (i < total) {
-        const int pos = static_cast<int>(i / nch), c = static_cast<int>(i - static_cast<size_t>(pos) * nch);
-        const int p = perm[pos];
-        const int t = p < T * k ? p / k : p - T * k;
-        v[u] = ld_nc16(x + (static_cast<size_t>(t) * H + 8 * c) * 2);
-        dst[u] = (static_cast<size_t>(pos) * H + 8 * c) * 2;
-      }
+      for (int u = 0; u < 8; ++u)
+        if (c0 + 32 * u < nch) v[u] = ld_nc16(src + 16 * (c0 + 32 * u));
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (c0 + 32 * u < nch) *reinterpret_cast<uint4*>(dst + 16 * (c0 + 32 * u)) = v[u];
     }
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-      if (base + stride * u < total) *reinterpret_cast<uint4*>(xs + dst[u]) = v[u];
   }
 }
 
@@ -741,18 +776,22 @@ bool tc_shape_ok(const moe_cfg_t& c) {
 
 bool tc_path_supported(const moe_cfg_t& c) { return tc_shape_ok(c) && encode_fn() != nullptr; }
 
-template <int N>
+template <int N, int MT>
 static size_t tc_smem13() {
-  constexpr uint32_t st = kTileA + N * 128;
-  constexpr int ns = (kSmemBudget - 128 * 17 * 4) / st > 8 ? 8 : (kSmemBudget - 128 * 17 * 4) / st;
-  return static_cast<size_t>(ns) * st + 128 * 17 * 4 + 1024;
+  constexpr uint32_t st = MT * kTileA + N * 128;
+  constexpr int stg = 128 * 17 * 4;
+  constexpr int ns = (kSmemBudget - stg) / st > 8 ? 8 : (kSmemBudget - stg) / st;
+  return static_cast<size_t>(ns) * st + stg + 1024;
 }
-template <int N>
+template <int N, int MT>
 static size_t tc_smem2() {
-  constexpr uint32_t st = kTileA + 2 * N * 128;
+  constexpr uint32_t st = MT * kTileA + 2 * N * 128;
   constexpr int ns = kSmemBudget / st > 8 ? 8 : kSmemBudget / st;
   return static_cast<size_t>(ns) * st + 1024;
 }
+
+// Two 128-row M-tiles per CTA: each token stage then feeds two accumulators.
+constexpr int kMT = 2;
 
 template <int N>
 static moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws, const WsLayout& L,
@@ -776,12 +815,10 @@ static moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uin
   const int gate_stride = c.has_shared_gate ? E + 1 : E;
   const uint64_t timeout = wait_timeout_ns();
 
-  tc_schedule_kernel<<<1, 1024, 0, st>>>(counts, offsets, E, I, Is, H, N, sched, sched + 1, t13, t2);
+  tc_schedule_kernel<<<1, 1024, 0, st>>>(counts, offsets, E, I, Is, H, N, kMT, kMT, sched, sched + 1, t13, t2);
   if (moe_status_t s = check_launch("tc_schedule_kernel")) return s;
   const int sms = sm_count();
-  const size_t gchunks = static_cast<size_t>(P) * (H / 8);
-  const int gg = static_cast<int>((gchunks + 255) / 256 < static_cast<size_t>(sms) * 8 ? (gchunks + 255) / 256
-                                                                                      : static_cast<size_t>(sms) * 8);
+  const int gg = (P + 7) / 8 < sms * 8 ? (P + 7) / 8 : sms * 8;
   tc_gather_kernel<<<gg, 256, 0, st>>>(static_cast<const uint8_t*>(p.x), perm, P, T, k, H, xs);
   if (moe_status_t s = check_launch("tc_gather_kernel")) return s;
 
@@ -800,17 +837,18 @@ static moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uin
             make_map(&mLoS, DT, alo, IsM, P, static_cast<uint64_t>(Imax) * 2, N);
   if (!ok) return set_error(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
 
-  const size_t s13 = tc_smem13<N>(), s2 = tc_smem2<N>();
-  cudaFuncSetAttribute(tc_w13_kernel<DT, N>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s13));
-  cudaFuncSetAttribute(tc_w2_kernel<DT, N>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s2));
+  const size_t s13 = tc_smem13<N, kMT>(), s2 = tc_smem2<N, kMT>();
+  cudaFuncSetAttribute(tc_w13_kernel<DT, N, kMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s13));
+  cudaFuncSetAttribute(tc_w2_kernel<DT, N, kMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s2));
   const int g13 = static_cast<int>(L.tc_max13 < sms ? L.tc_max13 : sms);
   const int g2 = static_cast<int>(L.tc_max2 < sms ? L.tc_max2 : sms);
-  tc_w13_kernel<DT, N><<<g13 > 0 ? g13 : 1, kTcThreads, s13, st>>>(mA, mAs, mB, t13, sched, H, I, Is, E, Imax, ahi,
-                                                                   alo, ctrl, timeout);
+  tc_w13_kernel<DT, N, kMT><<<g13 > 0 ? g13 : 1, kTcThreads, s13, st>>>(mA, mAs, mB, t13, sched, H, I, Is, E, Imax,
+                                                                       ahi, alo, ctrl, timeout);
   if (moe_status_t s = check_launch("tc_w13_kernel")) return s;
-  tc_w2_kernel<DT, N><<<g2 > 0 ? g2 : 1, kTcThreads, s2, st>>>(mW2, mW2s, mHi, mLo, mHiS, mLoS, t2, sched + 1, perm,
-                                                               p.topk_w, glog, gate_stride, c.has_shared_gate, T, H,
-                                                               I, Is, E, k, y, ctrl, timeout);
+  tc_w2_kernel<DT, N, kMT><<<g2 > 0 ? g2 : 1, kTcThreads, s2, st>>>(mW2, mW2s, mHi, mLo, mHiS, mLoS, t2, sched + 1,
+                                                                   perm, p.topk_w, glog, gate_stride,
+                                                                   c.has_shared_gate, T, H, I, Is, E, k, y, ctrl,
+                                                                   timeout);
   if (moe_status_t s = check_launch("tc_w2_kernel")) return s;
   stat_kernels(4);
   return MOE_OK;
