@@ -63,9 +63,9 @@ WsLayout ws_layout(const moe_cfg_t& c, int32_t T) {
   size_t off = sizeof(Control);
   L.ctrl = 0;
   L.ll_logits = off;
-  off = align_up(off + ((E + 2) & ~int64_t(1)) * 8, kWsAlign);
+  off = align_up(off + kLogitReplicas * ((E + 2) & ~int64_t(1)) * 8, kWsAlign);
   L.ll_act = off;
-  off = align_up(off + ((k * I + Is + 1) & ~int64_t(1)) * 8, kWsAlign);
+  off = align_up(off + kActReplicas * ((k * I + Is + 1) & ~int64_t(1)) * 8, kWsAlign);
   L.r_logits = off;
   off = align_up(off + static_cast<size_t>(T) * (E + 1) * 4, kWsAlign);
   if (T > 1) {

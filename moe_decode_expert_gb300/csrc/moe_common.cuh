@@ -69,6 +69,32 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
   return r;
 }
 
+// 16-byte load that the compiler keeps after every earlier volatile asm (in
+// particular after griddepcontrol.wait), for data an earlier kernel may write.
+__device__ __forceinline__ uint4 ld_ordered16(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p)
+               : "memory");
+  return r;
+}
+
+// L2-only prefetch of the 128-byte line holding p.  It never brings data into
+// L1, so it may precede griddepcontrol.wait even for data the preceding kernel
+// is still writing: L2 is the point of coherence and later reads see the write.
+__device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
+
+// 16-byte asynchronous copy global -> shared through L2 only (cp.async.cg);
+// completion is awaited per thread with cp_async_wait_all().  Both addresses
+// 16-byte aligned.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 __device__ __forceinline__ uint4 ld_nc16(const void* p) {
   uint4 r;
   asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -237,6 +263,57 @@ __device__ __forceinline__ void warp_topk_sorted8(const float* vals, int n, int 
   __syncwarp();
 }
 
+// ---- top-8 of up to 256 values by merging sorted lists across the warp.
+// Each value becomes a 64-bit key, (order_key(value) << 32) | ~index, so that a
+// larger key ranks first and equal values rank the lower index first; keys
+// are unique.  Padding keys are 0, below every real key.
+__device__ __forceinline__ uint64_t rank_key(float v, int idx) {
+  return (static_cast<uint64_t>(order_key(v)) << 32) | static_cast<uint32_t>(~idx);
+}
+__device__ __forceinline__ int rank_key_index(uint64_t key) { return static_cast<int>(~static_cast<uint32_t>(key)); }
+__device__ __forceinline__ void ce64(uint64_t& a, uint64_t& b) {  // a <- max, b <- min
+  const bool sw = b > a;
+  const uint64_t t = sw ? b : a;
+  b = sw ? a : b;
+  a = t;
+}
+// Sorts c[0..8) descending (bitonic merge network for a bitonic sequence).
+__device__ __forceinline__ void bitonic8_desc(uint64_t (&c)[8]) {
+  ce64(c[0], c[4]); ce64(c[1], c[5]); ce64(c[2], c[6]); ce64(c[3], c[7]);
+  ce64(c[0], c[2]); ce64(c[1], c[3]); ce64(c[4], c[6]); ce64(c[5], c[7]);
+  ce64(c[0], c[1]); ce64(c[2], c[3]); ce64(c[4], c[5]); ce64(c[6], c[7]);
+}
+// All 32 lanes end with c[0..8) = the 8 largest keys of vals[0..n), n <= 256,
+// sorted descending.  Lane l starts from indices l, l+32, ...; its 8 keys are
+// sorted (19-comparator network), then five rounds merge lane groups of 2, 4,
+// ..., 32: a lane keeps the top 8 of its list and its partner's (elementwise
+// max against the partner's list reversed gives a bitonic sequence holding
+// them, which one bitonic merge sorts).
+__device__ __forceinline__ void warp_top8_keys(const float* vals, int n, uint64_t (&c)[8]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    const int idx = s * 32 + lane;
+    const uint64_t key = rank_key(vals[idx < n ? idx : n - 1], idx);  // clamped load, no branch
+    c[s] = idx < n ? key : 0ull;
+  }
+  ce64(c[0], c[2]); ce64(c[1], c[3]); ce64(c[4], c[6]); ce64(c[5], c[7]);
+  ce64(c[0], c[4]); ce64(c[1], c[5]); ce64(c[2], c[6]); ce64(c[3], c[7]);
+  ce64(c[0], c[1]); ce64(c[2], c[3]); ce64(c[4], c[5]); ce64(c[6], c[7]);
+  ce64(c[2], c[4]); ce64(c[3], c[5]);
+  ce64(c[1], c[4]); ce64(c[3], c[6]);
+  ce64(c[1], c[2]); ce64(c[3], c[4]); ce64(c[5], c[6]);
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    uint64_t p[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) p[i] = __shfl_xor_sync(0xffffffffu, c[7 - i], m);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) c[i] = c[i] > p[i] ? c[i] : p[i];
+    bitonic8_desc(c);
+  }
+}
+
 // Routing weights for the k selected logits (sel[0] is the largest).  With
 // norm_topk: softmax over the k selected logits, which equals the full
 // softmax renormalised over the k.  Without: exp(l - max) / sum over all n.
@@ -280,55 +357,70 @@ __device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
   return v;
 }
 
+// One exchange word at p, or zero without a load when `pred` is false.
+__device__ __forceinline__ uint64_t ll_load1_pred(const uint64_t* p, bool pred) {
+  uint64_t w;
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\tmov.b64 %0, 0;\n\t"
+      "@q ld.relaxed.gpu.global.b64 %0, [%1];\n\t}"
+      : "=l"(w)
+      : "l"(p), "r"(static_cast<int>(pred)));
+  return w;
+}
+
+// Two exchange words at p, or zeros without a load when `pred` is false.
+__device__ __forceinline__ ulonglong2 ll_load2_pred(const uint64_t* p, bool pred) {
+  ulonglong2 w;
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %3, 0;\n\tmov.b64 %0, 0;\n\tmov.b64 %1, 0;\n\t"
+      "@q ld.relaxed.gpu.global.v2.b64 {%0,%1}, [%2];\n\t}"
+      : "=l"(w.x), "=l"(w.y)
+      : "l"(p), "r"(static_cast<int>(pred)));
+  return w;
+}
+
 // Gather n exchange words of this epoch into dst (fp32).  `nthr` threads
 // cooperate, this one being `tid`; word pairs are read with 16-byte loads
-// (the word array is padded to an even length).  Up to 2*kLLBatch words per
-// thread are requested back to back, so the common case costs one L2 round
-// trip; words not yet published are re-polled until `deadline`.  Returns
-// false if words were still missing then.
-constexpr int kLLBatch = 16;
+// (the word array is padded to an even length).  A thread requests all its
+// pairs (up to UM per round, predicated, no branches) back to back, so the
+// common case costs one L2 round trip; words not yet published are re-polled
+// until `deadline` (the retry loop is warp-uniform).  Returns false if words
+// were still missing then.
+template <int UM>
 __device__ __forceinline__ bool ll_gather(const uint64_t* src, float* dst, int n, int tid, int nthr,
                                           uint32_t epoch, uint64_t deadline) {
   const int npairs = (n + 1) >> 1;
-  for (int base = tid; base < npairs; base += nthr * kLLBatch) {
-    ulonglong2 w[kLLBatch];
+  const int U = (npairs + nthr - 1) / nthr;
+  for (int b0 = 0; b0 < U; b0 += UM) {
+    ulonglong2 w[UM];
+    uint32_t want = 0;
 #pragma unroll
-    for (int u = 0; u < kLLBatch; ++u) {
-      const int q = base + u * nthr;
-      if (q < npairs) w[u] = ll_load2(src + 2 * q);
+    for (int u = 0; u < UM; ++u) {
+      const int q = tid + nthr * (b0 + u);
+      const bool in = q < npairs;
+      want |= (in ? 1u : 0u) << u;
+      w[u] = ll_load2_pred(src + 2 * (in ? q : 0), in);
     }
-    uint32_t missing = 0;
+    for (;;) {
+      uint32_t missing = 0;
 #pragma unroll
-    for (int u = 0; u < kLLBatch; ++u) {
-      const int q = base + u * nthr;
-      if (q < npairs) {
+      for (int u = 0; u < UM; ++u) {
+        const int q = tid + nthr * (b0 + u);
         const bool ok0 = static_cast<uint32_t>(w[u].x >> 32) == epoch;
         const bool ok1 = 2 * q + 1 >= n || static_cast<uint32_t>(w[u].y >> 32) == epoch;
-        if (ok0 && ok1) {
-          dst[2 * q] = __uint_as_float(static_cast<uint32_t>(w[u].x));
-          if (2 * q + 1 < n) dst[2 * q + 1] = __uint_as_float(static_cast<uint32_t>(w[u].y));
-        } else {
-          missing |= 1u << u;
-        }
+        const bool wanted = (want >> u) & 1u;
+        const bool good = wanted && ok0 && ok1;
+        if (good) dst[2 * q] = __uint_as_float(static_cast<uint32_t>(w[u].x));
+        if (good && 2 * q + 1 < n) dst[2 * q + 1] = __uint_as_float(static_cast<uint32_t>(w[u].y));
+        missing |= (wanted && !good ? 1u : 0u) << u;
       }
-    }
-    while (missing) {
-      if (global_ns() > deadline) return false;
+      want = missing;
+      if (!__any_sync(0xffffffffu, want != 0u)) break;
+      if (__any_sync(0xffffffffu, global_ns() > deadline)) return false;
 #pragma unroll
-      for (int u = 0; u < kLLBatch; ++u)
-        if (missing & (1u << u)) w[u] = ll_load2(src + 2 * (base + u * nthr));
-#pragma unroll
-      for (int u = 0; u < kLLBatch; ++u) {
-        if (missing & (1u << u)) {
-          const int q = base + u * nthr;
-          const bool ok0 = static_cast<uint32_t>(w[u].x >> 32) == epoch;
-          const bool ok1 = 2 * q + 1 >= n || static_cast<uint32_t>(w[u].y >> 32) == epoch;
-          if (ok0 && ok1) {
-            dst[2 * q] = __uint_as_float(static_cast<uint32_t>(w[u].x));
-            if (2 * q + 1 < n) dst[2 * q + 1] = __uint_as_float(static_cast<uint32_t>(w[u].y));
-            missing &= ~(1u << u);
-          }
-        }
+      for (int u = 0; u < UM; ++u) {
+        const bool re = (want >> u) & 1u;
+        w[u] = ll_load2_pred(src + 2 * (re ? tid + nthr * (b0 + u) : 0), re);
       }
     }
   }

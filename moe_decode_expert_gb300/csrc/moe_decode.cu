@@ -50,22 +50,41 @@ struct DecodeArgs {
   float* topk_w;
   void* out;
   Control* ctrl;
-  uint64_t* ll_logits;
+  uint64_t* ll_logits;  // kLogitReplicas copies, ll_stride words apart
   uint64_t* ll_act;
   int H, E, k, I, Is, has_gate, norm_topk, out_dtype;
   int static_weights;  // MOE_FLAG_STATIC_WEIGHTS: weight reads may precede the PDL wait
-  uint32_t off_lg, off_act, off_w2;
+  int ll_stride;   // words between the copies of the logit words
+  int act_stride;  // words between the copies of the activation words
+  uint32_t rs_r, rs_s;  // shared-memory row strides (bytes) of the routed and shared W2 rows
+  uint32_t off_lg, off_act, off_terms, off_w2;
   uint64_t timeout_ns;
 };
 
+// 16-byte streaming load of a weight chunk, or zeros without a load when
+// `pred` is false (predicated, no branch).  Volatile, so loads issued before
+// griddepcontrol.wait really are issued there.
+__device__ __forceinline__ uint4 ld_stream16_pred(const void* p, bool pred) {
+  uint4 r;
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %5, 0;\n\tmov.b32 %0, 0;\n\tmov.b32 %1, 0;\n\tmov.b32 %2, 0;\n\t"
+      "mov.b32 %3, 0;\n\t@q ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];\n\t}"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p), "r"(static_cast<int>(pred)));
+  return r;
+}
+
 // Up to two weight rows of H 2-byte elements, streamed to registers 16 bytes
 // per lane per chunk (lane-strided, so a warp reads 512 contiguous bytes per
-// instruction), then dotted with x held in shared memory as fp32.
+// instruction), then dotted with x held in shared memory as fp32.  The code
+// is branch-free: chunks past the row end (and the second row of a one-row
+// unit) load as zeros, and four partial sums per row shorten the FMA chain.
 template <int DT>
 struct RowPair {
   const uint8_t* r0;
   const uint8_t* r1;
   int two;   // 1: two rows, 0: one row
+  int j;     // routed slot of the pair (phase 3)
   uint4 v0[kChunks], v1[kChunks];
 
   __device__ __forceinline__ void issue(int base, int nch, int lane) {
@@ -73,42 +92,113 @@ struct RowPair {
     for (int t = 0; t < kChunks; ++t) {
       const int c = base + lane + 32 * t;
       const bool in = c < nch;
-      v0[t] = in ? ld_stream16(r0 + 16 * static_cast<size_t>(c)) : make_uint4(0, 0, 0, 0);
-      v1[t] = (in && two) ? ld_stream16(r1 + 16 * static_cast<size_t>(c)) : make_uint4(0, 0, 0, 0);
+      const size_t off = 16 * static_cast<size_t>(in ? c : 0);
+      v0[t] = ld_stream16_pred(r0 + off, in);
+      v1[t] = ld_stream16_pred(r1 + off, in && two);
+    }
+  }
+
+  __device__ __forceinline__ void accumulate(const float* xs, int base, int nch, int lane, float (&a0)[4],
+                                             float (&a1)[4]) const {
+#pragma unroll
+    for (int t = 0; t < kChunks; ++t) {
+      const int c = min(base + lane + 32 * t, nch - 1);  // weights are zero past the end
+      const float4 xa = reinterpret_cast<const float4*>(xs)[2 * c];
+      const float4 xb = reinterpret_cast<const float4*>(xs)[2 * c + 1];
+      float f[8], h[8];
+      unpack8<DT>(v0[t], f);
+      unpack8<DT>(v1[t], h);
+      float& s0 = a0[t & 3];
+      float& s1 = a1[t & 3];
+      s0 = fmaf(f[0], xa.x, s0); s1 = fmaf(h[0], xa.x, s1);
+      s0 = fmaf(f[1], xa.y, s0); s1 = fmaf(h[1], xa.y, s1);
+      s0 = fmaf(f[2], xa.z, s0); s1 = fmaf(h[2], xa.z, s1);
+      s0 = fmaf(f[3], xa.w, s0); s1 = fmaf(h[3], xa.w, s1);
+      s0 = fmaf(f[4], xb.x, s0); s1 = fmaf(h[4], xb.x, s1);
+      s0 = fmaf(f[5], xb.y, s0); s1 = fmaf(h[5], xb.y, s1);
+      s0 = fmaf(f[6], xb.z, s0); s1 = fmaf(h[6], xb.z, s1);
+      s0 = fmaf(f[7], xb.w, s0); s1 = fmaf(h[7], xb.w, s1);
     }
   }
 
   // Completes the dot products whose first batch was issued with issue(0).
   __device__ __forceinline__ void finish(const float* xs, int nch, int lane, float& d0, float& d1) {
-    float a0 = 0.f, a1 = 0.f;
-    for (int base = 0; base < nch; base += 32 * kChunks) {
-      if (base) issue(base, nch, lane);
-#pragma unroll
-      for (int t = 0; t < kChunks; ++t) {
-        const int c = base + lane + 32 * t;
-        if (c < nch) {
-          const float4 xa = reinterpret_cast<const float4*>(xs)[2 * c];
-          const float4 xb = reinterpret_cast<const float4*>(xs)[2 * c + 1];
-          float f[8];
-          unpack8<DT>(v0[t], f);
-          a0 = fmaf(f[0], xa.x, a0); a0 = fmaf(f[1], xa.y, a0);
-          a0 = fmaf(f[2], xa.z, a0); a0 = fmaf(f[3], xa.w, a0);
-          a0 = fmaf(f[4], xb.x, a0); a0 = fmaf(f[5], xb.y, a0);
-          a0 = fmaf(f[6], xb.z, a0); a0 = fmaf(f[7], xb.w, a0);
-          if (two) {
-            unpack8<DT>(v1[t], f);
-            a1 = fmaf(f[0], xa.x, a1); a1 = fmaf(f[1], xa.y, a1);
-            a1 = fmaf(f[2], xa.z, a1); a1 = fmaf(f[3], xa.w, a1);
-            a1 = fmaf(f[4], xb.x, a1); a1 = fmaf(f[5], xb.y, a1);
-            a1 = fmaf(f[6], xb.z, a1); a1 = fmaf(f[7], xb.w, a1);
-          }
-        }
-      }
+    float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+    accumulate(xs, 0, nch, lane, a0, a1);
+    for (int base = 32 * kChunks; base < nch; base += 32 * kChunks) {  // rows longer than 4 KB
+      issue(base, nch, lane);
+      accumulate(xs, base, nch, lane, a0, a1);
     }
-    d0 = warp_sum(a0);
-    d1 = warp_sum(a1);
+    d0 = warp_sum((a0[0] + a0[1]) + (a0[2] + a0[3]));
+    d1 = warp_sum((a1[0] + a1[1]) + (a1[2] + a1[3]));
   }
 };
+
+// ---- W2 stage on the tensor cores (warp-level mma: the block is a GEMV over
+// 16-row tiles, far below tcgen05's 128-row tiles)
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+// 8-byte shared load, or zeros without a load when `pred` is false.
+__device__ __forceinline__ void lds64_pred(uint32_t addr, bool pred, uint32_t& x, uint32_t& y) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %3, 0;\n\tmov.b32 %0, 0;\n\tmov.b32 %1, 0;\n\t"
+      "@q ld.shared.v2.u32 {%0,%1}, [%2];\n\t}"
+      : "=r"(x), "=r"(y)
+      : "r"(addr), "r"(static_cast<int>(pred)));
+}
+template <int DT>
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  if constexpr (DT == MOE_BF16) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+}
+// Predicated 16-byte asynchronous copy global -> shared (no branch).
+__device__ __forceinline__ void cp_async16_pred(uint32_t dst, const void* src, bool pred) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t@q cp.async.cg.shared.global [%0], [%1], 16;\n\t}" ::"r"(dst),
+      "l"(src), "r"(static_cast<int>(pred))
+      : "memory");
+}
+
+
+// v = t0 + t1 + t2 in the storage type: t0 = rn(v), t1 = rn(v - t0),
+// t2 = rn(v - t0 - t1) (both differences are exact in fp32): about 24
+// significant bits in bf16.  term[s] packs term s of v.x (low half) and v.y.
+template <int DT>
+__device__ __forceinline__ void split3(float2 v, uint32_t (&term)[3]) {
+  float x = v.x, y = v.y;
+#pragma unroll
+  for (int s = 0; s < 3; ++s) {
+    uint32_t bx, by;
+    float rx, ry;
+    if constexpr (DT == MOE_BF16) {
+      const __nv_bfloat16 hx = __float2bfloat16_rn(x), hy = __float2bfloat16_rn(y);
+      bx = __bfloat16_as_ushort(hx); by = __bfloat16_as_ushort(hy);
+      rx = __bfloat162float(hx); ry = __bfloat162float(hy);
+    } else {
+      const __half hx = __float2half_rn(x), hy = __float2half_rn(y);
+      bx = __half_as_ushort(hx); by = __half_as_ushort(hy);
+      rx = __half2float(hx); ry = __half2float(hy);
+    }
+    term[s] = bx | (by << 16);
+    x -= rx;
+    y -= ry;
+  }
+}
 
 // DEPTH 1: one gate/up pair in flight per warp (<= 128 registers, two CTAs per
 // SM fit); DEPTH 2: two pairs in flight (one CTA per SM), for configs with more
@@ -116,19 +206,21 @@ struct RowPair {
 template <int DT, int DEPTH>
 __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(const DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) uint64_t bar;
   __shared__ int s_ids[32];
   __shared__ float s_sel[32];
   __shared__ float s_w[32];
   __shared__ float s_gate;
   __shared__ uint32_t s_epoch;
   __shared__ uint32_t s_fail;
-  __shared__ int s_second_arrive_done;
-  __shared__ volatile int s_ready[32];  // slot r ranked (its id is in s_ids[r])
+  __shared__ int s_next;                // next phase-3 work item of this CTA
+  __shared__ unsigned long long s_cand[64];  // per-warp top-k candidates (64-bit rank keys)
+  __shared__ volatile int s_wready;     // routing weights and gate are in s_w / s_gate
+  __shared__ float s_red[kDecWarps][64];
 
   float* xs = reinterpret_cast<float*>(smem);
   float* lg = reinterpret_cast<float*>(smem + a.off_lg);
   float* acts = reinterpret_cast<float*>(smem + a.off_act);
+  uint16_t* terms = reinterpret_cast<uint16_t*>(smem + a.off_terms);
   uint8_t* w2s = smem + a.off_w2;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -138,14 +230,62 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
   const int hn = static_cast<int>((static_cast<long long>(H) * (cta + 1)) / G) - h0;
   const size_t rowb = static_cast<size_t>(H) * 2;
   const int nch = H >> 3;
+  const int P = k * I;
+  const int K = P + Is;  // columns of the concatenated [routed | shared] activation vector
+  uint8_t* w2sh = w2s + static_cast<size_t>(k) * hn * a.rs_r;  // shared expert's rows
+  const uint32_t w2a = smem_u32(w2s), w2sha = smem_u32(w2sh);
+  const int mtiles = (hn + 15) >> 4;  // <= 4 (checked on the host)
+
+  // Phase 4 is split by columns: warp w owns the 16-column steps [ks0, ks1)
+  // of K.  It copies those columns of its W2 rows, gathers those activations
+  // and runs those tensor-core steps, so only the final sum crosses warps.
+  const int ksteps = (K + 15) >> 4;
+  const int kpw = (ksteps + kDecWarps - 1) / kDecWarps;
+  const int ks0 = min(warp * kpw, ksteps), ks1 = min(ks0 + kpw, ksteps);
+  const float inv_I = 1.0f / static_cast<float>(I);
+  // The expert slot (k = shared) and column within it of absolute column c.
+  auto locate = [&](int c, int& j, int& i) {
+    const int jr = min(k - 1, __float2int_rz((static_cast<float>(c) + 0.5f) * inv_I));
+    j = c < P ? jr : k;
+    i = c < P ? c - jr * I : c - P;
+  };
+  // Copies of this warp's W2 columns (routed: shared == false; shared expert:
+  // shared == true), expert block by expert block: within a block the rows x
+  // 16-byte chunks are spread over the lanes (flat index, fp32-reciprocal
+  // quotient, exact for these sizes).
+  const int wc0 = ks0 * 16, wc1 = min(ks1 * 16, K);  // this warp's columns
+  auto copy_w2_cols = [&](bool shared) {
+    int lo = shared ? max(wc0, P) : wc0;
+    const int hi = shared ? wc1 : min(wc1, P);
+    while (lo < hi) {
+      int j, i0;
+      locate(lo, j, i0);
+      const int seg = min(hi, j < k ? (j + 1) * I : K) - lo;  // columns in this block
+      const int nck = seg >> 3;                               // 16-byte chunks per row
+      const float inv = 1.0f / static_cast<float>(nck);
+      const uint32_t rs = j < k ? a.rs_r : a.rs_s;
+      const uint32_t dst0 = (j < k ? w2a + static_cast<uint32_t>(j * hn) * a.rs_r : w2sha) + 2 * i0;
+      const size_t srow = static_cast<size_t>(j < k ? I : Is) * 2;
+      const uint8_t* src0 = (j < k ? a.w2 + (static_cast<size_t>(s_ids[min(j, k - 1)]) * H + h0) * srow
+                                   : a.sw2 + static_cast<size_t>(h0) * srow) + 2 * i0;
+      for (int qq = lane; qq < hn * nck; qq += 32) {
+        const int r = __float2int_rz((static_cast<float>(qq) + 0.5f) * inv);
+        const int c = qq - r * nck;
+        cp_async16_pred(dst0 + static_cast<uint32_t>(r) * rs + 16 * c, src0 + r * srow + 16 * c, true);
+      }
+      lo += seg;
+    }
+  };
 
   if (tid == 0) {
-    mbar_init(&bar, 2);
-    mbar_fence_init();
     s_fail = 0;
-    s_second_arrive_done = 0;
-    for (int r = 0; r < 32; ++r) s_ready[r] = 0;
+    s_next = 0;
+    s_wready = 0;
   }
+  // x and the epoch word are read right after the PDL wait; start their DRAM
+  // trips now (into L2 only, so the wait still orders the reads that count).
+  if (tid < ((H * 2 + 127) >> 7)) prefetch_l2(a.x + 128 * static_cast<size_t>(tid));
+  if (tid == kDecThreads - 1) prefetch_l2(&a.ctrl->gen);
   pdl_launch_dependents();
   __syncthreads();
 
@@ -167,83 +307,100 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
       rp.two = 1;
     }
   };
-  auto issue_shared_w2 = [&]() {  // thread 0: the shared expert's W2 rows of this CTA's slice
-    if (Is > 0 && hn > 0) {
-      const uint32_t bytes = static_cast<uint32_t>(hn) * Is * 2;
-      mbar_arrive_expect_tx(&bar, bytes);
-      bulk_g2s(w2s + static_cast<size_t>(k) * hn * I * 2, a.sw2 + static_cast<size_t>(h0) * Is * 2, bytes, &bar);
-    } else {
-      mbar_arrive(&bar);
-    }
-  };
   if (a.static_weights) {
     if (u < n1) { setup_unit(u); rp.issue(0, nch, lane); }
-    if (tid == 0) issue_shared_w2();
+    if (Is > 0) copy_w2_cols(true);
   }
   pdl_wait();  // x (and anything else an earlier kernel wrote) is visible from here
   if (!a.static_weights && u < n1) { setup_unit(u); rp.issue(0, nch, lane); }
 
+  uint32_t gen_prev = 0;
+  if (tid == 0) gen_prev = ld_relaxed_u32(&a.ctrl->gen);  // in flight together with x
   for (int c = tid; c < nch; c += kDecThreads) {
     float f[8];
-    unpack8<DT>(ld_nc16(a.x + 16 * static_cast<size_t>(c)), f);
+    unpack8<DT>(ld_ordered16(a.x + 16 * static_cast<size_t>(c)), f);
     reinterpret_cast<float4*>(xs)[2 * c] = make_float4(f[0], f[1], f[2], f[3]);
     reinterpret_cast<float4*>(xs)[2 * c + 1] = make_float4(f[4], f[5], f[6], f[7]);
   }
   if (tid == 0) {
-    uint32_t ep = ld_relaxed_u32(&a.ctrl->gen) + 1u;
+    uint32_t ep = gen_prev + 1u;
     s_epoch = ep ? ep : 1u;
     // The arrival counter of the other parity was last used by the previous
     // launch, which has completed; clear it for the next launch.
     if (cta == 0) atomicExch(&a.ctrl->arrive[(s_epoch + 1u) & 1u], 0u);
-    if (!a.static_weights) issue_shared_w2();
   }
+  if (!a.static_weights && Is > 0) copy_w2_cols(true);
   __syncthreads();
   const uint32_t epoch = s_epoch;
 
+  // Every CTA reads all logits and every activation, so each word is
+  // published in several copies (readers spread over more L2 lines).
   while (u < n1) {
     float d0, d1;
     rp.finish(xs, nch, lane, d0, d1);
-    if (lane == 0) {
-      if (u < E + a.has_gate) ll_store(a.ll_logits + u, d0, epoch);
-      else ll_store(a.ll_act + static_cast<size_t>(k) * I + (u - E - a.has_gate), silu_f(d0) * d1, epoch);
+    if (u < E + a.has_gate) {
+      if (lane < kLogitReplicas) ll_store(a.ll_logits + static_cast<size_t>(lane) * a.ll_stride + u, d0, epoch);
+    } else if (lane < kActReplicas) {
+      ll_store(a.ll_act + static_cast<size_t>(lane) * a.act_stride + P + (u - E - a.has_gate), silu_f(d0) * d1,
+               epoch);
     }
     q += kDecWarps;
     u = q * G + cta;
     if (u < n1) { setup_unit(u); rp.issue(0, nch, lane); }
   }
 
-  // ---- phase 2 (warp 0): gather the logits and rank them.  Each ranked
-  // expert is published to the other warps, and its W2 rows requested, as
-  // soon as its round ends, so expert loads overlap the rest of the ranking.
-  if (warp == 0) {
+  // ---- phase 2: the logits, their top-k (fp32, lower index first on ties)
+  // and the routing weights.  Warp w reads logits 32w..32w+31 (one exchange
+  // word per lane; the gate logit rides along at index E) and keeps its own
+  // top-k by k rounds of warp max + lowest lane; the 8 warps' candidates are
+  // then ranked exactly by all threads (4 threads per candidate, 64-bit keys
+  // (logit key, ~index) are unique), and candidate rank r < k fills slot r.
+  if (E <= 256 && k <= 8) {
+    if (warp == 0) {  // one warp polls the words (all warps polling floods L2)
+      const uint64_t* src = a.ll_logits + static_cast<size_t>(cta % kLogitReplicas) * a.ll_stride;
+      const bool ok = ll_gather<8>(src, lg, E + a.has_gate, lane, 32, epoch, global_ns() + a.timeout_ns);
+      if (!__all_sync(0xffffffffu, ok) && lane == 0) s_fail = kDevTimeoutLogits;
+    }
+    __syncthreads();
+    const int i0 = warp * 32 + lane;
+    const float v0 = lg[min(i0, E - 1)];              // clamped load, no branch
+    uint32_t key = i0 < E ? order_key(v0) : 0u;       // finite logits have keys > 0
+    uint64_t mine = 0;
+    for (int r = 0; r < k; ++r) {
+      const uint32_t m = __reduce_max_sync(0xffffffffu, key);
+      const uint32_t b = __ballot_sync(0xffffffffu, key == m && key != 0u);
+      const int wl = __ffs(b) - 1;
+      mine = (lane == r && b) ? (static_cast<uint64_t>(m) << 32) | static_cast<uint32_t>(~(warp * 32 + wl)) : mine;
+      key = lane == wl ? 0u : key;
+    }
+    if (lane < 8) s_cand[warp * 8 + lane] = mine;
+    __syncthreads();
+    {
+      const int c = tid >> 2, q4 = tid & 3;
+      const uint64_t kc = s_cand[c];
+      int cnt = 0;
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj) cnt += s_cand[q4 * 16 + jj] > kc ? 1 : 0;
+      cnt += __shfl_xor_sync(0xffffffffu, cnt, 1);
+      cnt += __shfl_xor_sync(0xffffffffu, cnt, 2);
+      if (q4 == 0 && kc != 0ull && cnt < k) {
+        const int id = rank_key_index(kc);
+        s_ids[cnt] = id;
+        s_sel[cnt] = lg[id];
+      }
+    }
+  } else if (warp == 0) {
+    // many experts or k > 8: one warp gathers all logits and ranks them
     const int nl = E + a.has_gate;
-    const bool ok = ll_gather(a.ll_logits, lg, nl, lane, 32, epoch, global_ns() + a.timeout_ns);
-    if (__all_sync(0xffffffffu, ok)) {
-      const uint32_t bytes = static_cast<uint32_t>(hn) * I * 2;
-      if (lane == 0) {
-        if (hn > 0) mbar_arrive_expect_tx(&bar, bytes * k);
-        else mbar_arrive(&bar);
-        s_second_arrive_done = 1;
-      }
-      __syncwarp();
-      auto publish = [&](int r) {
-        if (lane == 0) {
-          __threadfence_block();
-          s_ready[r] = 1;
-        }
-      };
-      if (E <= 256) {
-        warp_topk_sorted8(lg, E, k, s_ids, s_sel, publish);
-      } else {
-        warp_topk<32>(lg, E, k, s_ids, s_sel);
-        __syncwarp();
-        for (int r = 0; r < k; ++r) publish(r);
-      }
-      __syncwarp();
-      // this CTA's W2 rows of the k experts, one lane per expert
-      if (hn > 0 && lane < k)
-        bulk_g2s(w2s + static_cast<size_t>(lane) * hn * I * 2,
-                 a.w2 + (static_cast<size_t>(s_ids[lane]) * H + h0) * I * 2, bytes, &bar);
+    const uint64_t* src = a.ll_logits + static_cast<size_t>(cta % kLogitReplicas) * a.ll_stride;
+    const bool ok = ll_gather<8>(src, lg, nl, lane, 32, epoch, global_ns() + a.timeout_ns);
+    if (__all_sync(0xffffffffu, ok)) warp_topk<32>(lg, E, k, s_ids, s_sel);
+    else if (lane == 0) s_fail = kDevTimeoutLogits;
+  }
+  __syncthreads();
+  const bool ranked = s_fail == 0;  // uniform: read after the barrier
+  if (warp == 0) {
+    if (ranked) {
       warp_routing_weights(lg, E, s_sel, k, a.norm_topk, s_w);
       if (lane == 0) s_gate = a.has_gate ? sigmoid_f(lg[E]) : 1.0f;
       __syncwarp();
@@ -251,153 +408,252 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
         a.topk_ids[lane] = s_ids[lane];
         a.topk_w[lane] = s_w[lane];
       }
-    } else if (lane == 0) {
-      s_fail = kDevTimeoutLogits;
+    }
+    if (lane == 0) {
       __threadfence_block();
-      for (int r = 0; r < 32; ++r) s_ready[r] = 1;  // let the waiting warps see the failure
+      s_wready = 1;
     }
   }
 
-  // ---- phase 3: this CTA's share of the k*I routed gate/up pairs; a warp
-  // starts a pair as soon as the pair's expert has been ranked.  With
-  // DEPTH == 2 a warp keeps two pairs' rows in flight at once.
-  const int P = k * I;
-  auto wait_slot = [&](int j) -> bool {
+  // ---- phase 3: this CTA's share of the k*I routed gate/up pairs.  Warps
+  // take pairs in order from a shared counter, so warp 0 (busy ranking) only
+  // picks up what is left; each activation is published already multiplied
+  // by its routing weight.  With DEPTH == 2 a warp keeps two pairs' rows in
+  // flight at once.  A warp copies its W2 columns of the selected experts
+  // while its first pair's rows are in flight.
+  auto wait_flag = [&](volatile int* f) -> bool {
     const uint64_t deadline = global_ns() + a.timeout_ns;
-    while (s_ready[j] == 0) {
+    while (*f == 0) {
       if (global_ns() > deadline) return false;
       __nanosleep(32);
     }
     __threadfence_block();
     return true;
   };
-  auto start_pair = [&](RowPair<DT>& r, int p) -> bool {
+  auto grab = [&](int n) -> int {
+    int v = 0;
+    if (lane == 0) v = atomicAdd(&s_next, n);
+    return __shfl_sync(0xffffffffu, v, 0);
+  };
+  auto start_pair = [&](RowPair<DT>& r, int p) {
     const int j = p / I, i = p - j * I;
-    if (!wait_slot(j)) {
-      if (lane == 0) s_fail = kDevTimeoutLogits;
-      return false;
-    }
-    if (s_fail) return false;
     const size_t erow = static_cast<size_t>(s_ids[j]) * 2 * I;
     r.r0 = a.w13 + (erow + i) * rowb;
     r.r1 = a.w13 + (erow + I + i) * rowb;
     r.two = 1;
+    r.j = j;
     r.issue(0, nch, lane);
-    return true;
   };
-  auto end_pair = [&](RowPair<DT>& r, int p) {
+  auto end_pair = [&](RowPair<DT>& r, int p) -> bool {
     float g, up;
     r.finish(xs, nch, lane, g, up);
-    if (lane == 0) ll_store(a.ll_act + p, silu_f(g) * up, epoch);
+    if (!wait_flag(&s_wready)) {
+      if (lane == 0) s_fail = kDevTimeoutLogits;
+      return false;
+    }
+    if (lane < kActReplicas) ll_store(a.ll_act + static_cast<size_t>(lane) * a.act_stride + p, silu_f(g) * up * s_w[r.j], epoch);
+    return true;
   };
-  if constexpr (DEPTH == 2) {
-    RowPair<DT> rq;
-    for (int qq = warp;; qq += 2 * kDecWarps) {
-      const int pa = qq * G + cta, pb = (qq + kDecWarps) * G + cta;
-      if (pa >= P) break;
-      if (!start_pair(rp, pa)) break;
-      const bool has_b = pb < P && start_pair(rq, pb);
-      end_pair(rp, pa);
-      if (!has_b) break;
-      end_pair(rq, pb);
+  if (ranked && !s_fail) {
+    bool copied = false;
+    if constexpr (DEPTH == 2) {
+      RowPair<DT> rq;
+      for (;;) {
+        const int qq = grab(2);
+        const int pa = qq * G + cta, pb = (qq + 1) * G + cta;
+        if (pa >= P) break;
+        start_pair(rp, pa);
+        if (pb < P) start_pair(rq, pb);
+        if (!copied) { copy_w2_cols(false); copied = true; }
+        if (!end_pair(rp, pa) || pb >= P) break;
+        if (!end_pair(rq, pb)) break;
+      }
+    } else {
+      for (;;) {
+        const int p = grab(1) * G + cta;
+        if (p >= P) break;
+        start_pair(rp, p);
+        if (!copied) { copy_w2_cols(false); copied = true; }
+        if (!end_pair(rp, p)) break;
+      }
     }
-  } else {
-    for (int qq = warp;; qq += kDecWarps) {
-      const int p = qq * G + cta;
-      if (p >= P) break;
-      if (!start_pair(rp, p)) break;
-      end_pair(rp, p);
-    }
+    if (!copied) copy_w2_cols(false);
   }
 
-  {
-    // ---- phase 4: all activations, this CTA's W2 rows, out slice
-    // One thread per CTA counts CTAs in and waits for all G of them; only then
-    // do all threads read the exchange words (one pass when they have landed;
-    // the epoch tags still catch any word not yet visible).  Polling the words
-    // themselves from every thread of every CTA congests the L2 lines they
-    // live in and delays the producers' stores.
-    __syncthreads();
-    bool ok = true;
-    if (tid == 0 && !s_fail) {
-      uint32_t* cnt = &a.ctrl->arrive[epoch & 1u];
-      atomicAdd(cnt, 1u);
-      const uint64_t deadline = global_ns() + a.timeout_ns;
-      while (ld_relaxed_u32(cnt) < static_cast<uint32_t>(G)) {
-        if (global_ns() > deadline) { ok = false; break; }
-      }
-      if (!ok) s_fail = kDevTimeoutAct;
+  // ---- phase 4 (per warp): this warp's activations and W2 columns
+  // The warp reads the exchange words of its columns (all requested at once,
+  // re-polling any not yet published) into its range of `acts`, writes the
+  // three storage-type terms of each activation (split3; the routed ones
+  // already weighted, the shared ones times the gate here; fp16 scaled by a
+  // power of two that puts the range's largest magnitude in [2^14, 2^15),
+  // exact and undone on the sums) in B-fragment order, then runs its
+  // tensor-core steps: out[h0 + r] = sum over the K columns of W2 row r times
+  // the activations, A = 16 W2 rows x 16 columns (ldmatrix from the padded
+  // rows), B columns 0-2 = the activation terms, fp32 accumulation.  Lane t of
+  // a B fragment needs columns 2t, 2t+1, 2t+8, 2t+9 of a step, kept at
+  // 4t..4t+3 of the step's 16 slots.
+  cp_async_wait_all();  // this thread's W2 copies
+  // One thread per CTA counts CTAs in and waits for all G of them before any
+  // warp reads the activation words: every warp polling the words while other
+  // CTAs are still producing floods L2 with re-reads and slows the weight
+  // streams.  After the count the words have (nearly always) landed and each
+  // warp's gather is one round trip (the epoch tags still catch a late one).
+  __syncthreads();
+  if (tid == 0 && !s_fail) {
+    uint32_t* cnt = &a.ctrl->arrive[epoch & 1u];
+    atomicAdd(cnt, 1u);
+    const uint64_t deadline = global_ns() + a.timeout_ns;
+    bool arrived = true;
+    while (ld_relaxed_u32(cnt) < static_cast<uint32_t>(G)) {
+      if (global_ns() > deadline) { arrived = false; break; }
     }
-    __syncthreads();
-    if (!s_fail) ok = ll_gather(a.ll_act, acts, P + Is, tid, kDecThreads, epoch, global_ns() + a.timeout_ns);
-    if (!ok) s_fail = kDevTimeoutAct;
-    if (tid == 0 && !mbar_wait_until(&bar, 0, global_ns() + a.timeout_ns)) s_fail = kDevTimeoutCopy;
-    __syncthreads();
-    if (!s_fail) {
-      // Fold the routing weight (and the shared gate) into the activations,
-      // so each output is one dot product over the concatenated
-      // [k*I routed | Is shared] activation vector.  Integer quotients come
-      // from an fp32 reciprocal, exact for indices below 2^22.
-      const float inv_I = 1.0f / static_cast<float>(I);
-      for (int i = tid; i < P + Is; i += kDecThreads) {
-        const int j = i < P ? __float2int_rz((static_cast<float>(i) + 0.5f) * inv_I) : k;
-        acts[i] *= j < k ? s_w[j] : s_gate;
+    if (!arrived) s_fail = kDevTimeoutAct;
+  }
+  __syncthreads();
+  {
+    const int g = lane >> 2, t = lane & 3;
+    const int c0 = ks0 * 16, c1 = min(ks1 * 16, K);
+    const int Kp = ksteps * 16;
+    bool ok = __all_sync(0xffffffffu, s_fail == 0);  // warp-uniform
+    if (ok && c1 > c0) {
+      const uint64_t* rep = a.ll_act + static_cast<size_t>(cta % kActReplicas) * a.act_stride + c0;
+      const uint64_t dl = global_ns() + a.timeout_ns;
+      const bool got = ((c1 - c0 + 1) >> 1) <= 4 * 32 ? ll_gather<4>(rep, acts + c0, c1 - c0, lane, 32, epoch, dl)
+                                                     : ll_gather<16>(rep, acts + c0, c1 - c0, lane, 32, epoch, dl);
+      ok = __all_sync(0xffffffffu, got);
+      if (!ok && lane == 0) s_fail = kDevTimeoutAct;
+    }
+    __syncwarp();
+    float unsc = 1.0f;
+    if (ok && ks1 > ks0) {
+      const float gate = s_gate;
+      const float2* acts2 = reinterpret_cast<const float2*>(acts);
+      float sc = 1.0f;
+      if constexpr (DT == MOE_F16) {
+        float mx = 0.0f;
+        for (int qp = (c0 >> 1) + lane; 2 * qp < c1; qp += 32) {
+          const float2 v = acts2[qp];
+          const float f = 2 * qp >= P ? gate : 1.0f;
+          mx = fmaxf(mx, fmaxf(fabsf(v.x * f), fabsf(v.y * f)));
+        }
+        const uint32_t amax = __reduce_max_sync(0xffffffffu, __float_as_uint(mx));
+        int sh = amax ? 14 - (static_cast<int>(amax >> 23) - 127) : 0;
+        sh = max(-100, min(100, sh));
+        sc = __int_as_float((127 + sh) << 23);
+        unsc = __int_as_float((127 - sh) << 23);
       }
-      __syncthreads();
-      // Two output rows per warp, 16 threads per row; thread tl takes chunks
-      // tl, tl+16, ... (16-byte chunks of 8 weights) into four independent
-      // accumulators.  The loop bound is warp-uniform so every lane reaches the
-      // shuffles.
-      const int cpe = I >> 3;
-      const int nchunk = (P + Is) >> 3;
-      const float inv_cpe = 1.0f / static_cast<float>(cpe);
-      const int tl = tid & 15;
-      for (int rbase = warp * 2; rbase < hn; rbase += kDecThreads / 16) {
-        const int r = rbase + ((tid >> 4) & 1);
-        const bool active = r < hn;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        if (active) {
-          const uint8_t* rrow = w2s + static_cast<size_t>(r) * I * 2;
-          const uint8_t* srow = w2s + (static_cast<size_t>(k) * hn * I + static_cast<size_t>(r) * Is) * 2;
-          for (int c0 = tl; c0 < nchunk; c0 += 64) {
+      for (int qp = (c0 >> 1) + lane; 2 * qp < ks1 * 16; qp += 32) {
+        const int pcol = 2 * qp;
+        const float2 v0 = acts2[min(qp, (K >> 1) - 1)];  // clamped load, no branch
+        const float f = pcol < K ? (pcol >= P ? gate : 1.0f) * sc : 0.0f;
+        uint32_t tm[3];
+        split3<DT>(make_float2(v0.x * f, v0.y * f), tm);
+        const int w = pcol & 15;
+        const int at = (pcol & ~15) + (w < 8 ? 2 * w : 2 * w - 14);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int c = c0 + 16 * u;
-              if (c < nchunk) {
-                const int j = __float2int_rz((static_cast<float>(c) + 0.5f) * inv_cpe);
-                const uint8_t* wp = j < k ? rrow + (static_cast<size_t>(j) * hn * I + (c - j * cpe) * 8) * 2
-                                          : srow + static_cast<size_t>(c - k * cpe) * 16;
-                const uint4 v = *reinterpret_cast<const uint4*>(wp);
-                const float4 xa = reinterpret_cast<const float4*>(acts)[2 * c];
-                const float4 xb = reinterpret_cast<const float4*>(acts)[2 * c + 1];
-                float f[8];
-                unpack8<DT>(v, f);
-                float t = f[0] * xa.x;
-                t = fmaf(f[1], xa.y, t); t = fmaf(f[2], xa.z, t); t = fmaf(f[3], xa.w, t);
-                t = fmaf(f[4], xb.x, t); t = fmaf(f[5], xb.y, t); t = fmaf(f[6], xb.z, t);
-                t = fmaf(f[7], xb.w, t);
-                acc[u] += t;
-              }
-            }
+        for (int e = 0; e < 3; ++e) *reinterpret_cast<uint32_t*>(terms + static_cast<size_t>(e) * Kp + at) = tm[e];
+      }
+    }
+    __syncwarp();  // terms and this warp's W2 copies visible to all its lanes
+    const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8;
+    const uint32_t ta0 = smem_u32(terms) + static_cast<uint32_t>(g * Kp + 4 * t) * 2;
+    const bool bl = lane < 12;  // lanes holding B columns 0-2
+    float acc[4][4], acc1[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.0f;
+    acc1[0] = acc1[1] = acc1[2] = acc1[3] = 0.0f;
+    if (ok && mtiles == 1 && (I & 15) == 0 && (Is & 15) == 0) {
+      // One 16-row tile; expert blocks are whole 16-column steps, so the
+      // warp walks them as uniform segments with plain pointer increments,
+      // four steps of loads in flight and two accumulator chains.
+      const int row = min(lrow, hn - 1);
+      const uint32_t lk = (lane >> 4) * 16;
+      const uint32_t roff_r = static_cast<uint32_t>(row) * a.rs_r + lk;
+      const uint32_t roff_s = static_cast<uint32_t>(row) * a.rs_s + lk;
+      const int spe = I >> 4, psteps = P >> 4;
+      uint32_t ta = ta0 + static_cast<uint32_t>(ks0) * 32;
+      int ks = ks0;
+      while (ks < ks1) {
+        const int j = ks < psteps ? ks / spe : k;
+        const int send = min(ks1, j < k ? (j + 1) * spe : ksteps);
+        uint32_t ap = j < k ? w2a + static_cast<uint32_t>(j * hn) * a.rs_r + roff_r + (ks - j * spe) * 32
+                            : w2sha + roff_s + (ks - psteps) * 32;
+        for (; ks + 4 <= send; ks += 4) {
+          uint32_t b[4][2], av[4][4];
+#pragma unroll
+          for (int v = 0; v < 4; ++v) lds64_pred(ta + 32 * v, bl, b[v][0], b[v][1]);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) ldsm_x4(ap + 32 * v, av[v][0], av[v][1], av[v][2], av[v][3]);
+          mma16816<DT>(acc[0], av[0][0], av[0][1], av[0][2], av[0][3], b[0][0], b[0][1]);
+          mma16816<DT>(acc1, av[1][0], av[1][1], av[1][2], av[1][3], b[1][0], b[1][1]);
+          mma16816<DT>(acc[0], av[2][0], av[2][1], av[2][2], av[2][3], b[2][0], b[2][1]);
+          mma16816<DT>(acc1, av[3][0], av[3][1], av[3][2], av[3][3], b[3][0], b[3][1]);
+          ap += 128;
+          ta += 128;
+        }
+        for (; ks < send; ++ks) {
+          uint32_t b0, b1, a0, a1, a2, a3;
+          lds64_pred(ta, bl, b0, b1);
+          ldsm_x4(ap, a0, a1, a2, a3);
+          mma16816<DT>(acc[0], a0, a1, a2, a3, b0, b1);
+          ap += 32;
+          ta += 32;
+        }
+      }
+    } else if (ok) {
+      // General shapes: up to four 16-row tiles; each lane locates the expert
+      // block and column of its 8-column chunk at every step.
+      for (int ks = ks0; ks < ks1; ++ks) {
+        uint32_t b0, b1;
+        lds64_pred(ta0 + static_cast<uint32_t>(ks) * 32, bl, b0, b1);
+        int j, i;
+        locate(min(ks * 16 + (lane >> 4) * 8, K - 8), j, i);  // columns past K meet zeros in B
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          if (m < mtiles) {
+            const int row = min(m * 16 + lrow, hn - 1);
+            const uint32_t ap = j < k ? w2a + static_cast<uint32_t>(j * hn + row) * a.rs_r + 2 * i
+                                      : w2sha + static_cast<uint32_t>(row) * a.rs_s + 2 * i;
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(ap, a0, a1, a2, a3);
+            mma16816<DT>(acc[m], a0, a1, a2, a3, b0, b1);
           }
         }
-        float sum = (acc[0] + acc[1]) + (acc[2] + acc[3]);
-#pragma unroll
-        for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        if (active && tl == 0) store_out(a.out, h0 + r, sum, a.out_dtype);
       }
-      // Every CTA has read the epoch before publishing its activations and CTA 0
-      // has now seen all of them, so the next launch may use the next epoch.
-      if (cta == 0 && tid == 0) atomicExch(&a.ctrl->gen, epoch);
-      return;
+    }
+    // columns 0, 1 (lane t = 0) and 2 (lane t = 1) of rows g and g + 8
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      float top = acc[m][0] + acc[m][1], bot = acc[m][2] + acc[m][3];
+      if (m == 0) {  // the fast path's second accumulator chain (zeros otherwise)
+        top += acc1[0] + acc1[1];
+        bot += acc1[2] + acc1[3];
+      }
+      top += __shfl_xor_sync(0xffffffffu, top, 1);
+      bot += __shfl_xor_sync(0xffffffffu, bot, 1);
+      if (t == 0) {
+        s_red[warp][m * 16 + g] = top * unsc;
+        s_red[warp][m * 16 + g + 8] = bot * unsc;
+      }
     }
   }
-
-  // ---- failure path: record, let this CTA's own bulk copies land, bump the epoch
+  __syncthreads();
+  if (!s_fail) {
+    if (tid < hn) {
+      float sum = 0.0f;
+#pragma unroll
+      for (int w = 0; w < kDecWarps; ++w) sum += s_red[w][tid];
+      store_out(a.out, h0 + tid, sum, a.out_dtype);
+    }
+    // Every CTA has read the epoch before publishing its activations and CTA 0
+    // has now seen all of them, so the next launch may use the next epoch.
+    if (cta == 0 && tid == 0) atomicExch(&a.ctrl->gen, epoch);
+    return;
+  }
+  // ---- failure path: record the error and bump the epoch (every thread's
+  // W2 copies have landed: cp_async_wait_all above)
   if (tid == 0) {
     report_error(a.ctrl, s_fail, static_cast<uint32_t>(cta));
-    if (!s_second_arrive_done) mbar_arrive(&bar);
-    mbar_wait_until(&bar, 0, global_ns() + a.timeout_ns);
     if (cta == 0) atomicExch(&a.ctrl->gen, epoch);
   }
 }
@@ -412,24 +668,32 @@ int decode_grid(const moe_cfg_t& c) {
   return g < 1 ? 1 : g;
 }
 
+// Shared-memory row stride (bytes) of n 2-byte elements: an odd number of
+// 16-byte units, so that 8 consecutive rows start in 8 different bank groups
+// (conflict-free ldmatrix).
+static uint32_t w2_row_stride(int n) { return static_cast<uint32_t>(((n / 8) | 1) * 16); }
+
 static void decode_smem_layout(const moe_cfg_t& c, int G, uint32_t& off_lg, uint32_t& off_act,
-                               uint32_t& off_w2, size_t& total) {
+                               uint32_t& off_terms, uint32_t& off_w2, size_t& total) {
   const size_t H = c.hidden, E = c.n_experts, k = c.top_k, I = c.inter, Is = c.shared_inter;
   const size_t hn_max = (H + G - 1) / G;
+  const size_t Kp = (k * I + Is + 15) / 16 * 16;
   size_t off = align_up(H * 4, 128);
   off_lg = static_cast<uint32_t>(off);
   off += align_up((E + 2) * 4, 128);
   off_act = static_cast<uint32_t>(off);
-  off += align_up((k * I + Is + 2) * 4, 128);
+  off += align_up((Kp + 2) * 4, 128);
+  off_terms = static_cast<uint32_t>(off);
+  off += align_up(3 * Kp * 2, 128);
   off_w2 = static_cast<uint32_t>(off);
-  off += align_up(hn_max * (k * I + Is) * 2, 128);
+  off += align_up(hn_max * (k * w2_row_stride(c.inter) + (Is ? w2_row_stride(c.shared_inter) : 0)), 128);
   total = off;
 }
 
 size_t decode_smem_bytes(const moe_cfg_t& c, int G) {
-  uint32_t a, b, d;
+  uint32_t a, b, d, e;
   size_t t;
-  decode_smem_layout(c, G, a, b, d, t);
+  decode_smem_layout(c, G, a, b, d, e, t);
   return t;
 }
 
@@ -482,11 +746,18 @@ moe_status_t launch_decode_fused(const moe_cfg_t& c, const BlockPtrs& p, uint8_t
   a.H = c.hidden; a.E = c.n_experts; a.k = c.top_k; a.I = c.inter; a.Is = c.shared_inter;
   a.has_gate = c.has_shared_gate; a.norm_topk = c.norm_topk; a.out_dtype = c.out_dtype;
   a.static_weights = (c.flags & MOE_FLAG_STATIC_WEIGHTS) ? 1 : 0;
+  a.ll_stride = (c.n_experts + 2) & ~1;
+  a.act_stride = (c.top_k * c.inter + c.shared_inter + 1) & ~1;
+  a.rs_r = w2_row_stride(c.inter);
+  a.rs_s = w2_row_stride(c.shared_inter);
   size_t smem;
-  decode_smem_layout(c, G, a.off_lg, a.off_act, a.off_w2, smem);
+  decode_smem_layout(c, G, a.off_lg, a.off_act, a.off_terms, a.off_w2, smem);
   a.timeout_ns = wait_timeout_ns();
   if (smem > 227 * 1024)
     return set_error(MOE_ERR_UNSUPPORTED, "decode: needs %zu B of shared memory per CTA (max 232448)", smem);
+  if ((c.hidden + G - 1) / G > 64)
+    return set_error(MOE_ERR_UNSUPPORTED, "decode: %d output rows per CTA (hidden / CTAs) exceed 64",
+                     (c.hidden + G - 1) / G);
   // two pairs in flight per warp when a CTA has more routed pairs than warps
   const bool deep = (c.top_k * c.inter + G - 1) / G > kDecWarps;
   if (c.dtype == MOE_BF16)

@@ -11,14 +11,19 @@
 namespace moe {
 
 constexpr size_t kWsAlign = 256;
+// Copies of the router-logit exchange words of the single-launch decode (each
+// CTA reads one copy, so fewer CTAs poll each L2 line).
+constexpr int kLogitReplicas = 8;
+// Copies of the activation exchange words (each CTA reads one copy).
+constexpr int kActReplicas = 4;
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Byte offsets of every region of one workspace, for `T` tokens of a cfg.
 struct WsLayout {
   size_t ctrl = 0;        // Control block, 256 B
   // single-launch decode (T == 1): exchange words between CTAs
-  size_t ll_logits = 0;   // (E + 1) words of 8 B, padded to even
-  size_t ll_act = 0;      // (k*I + Is) words
+  size_t ll_logits = 0;   // kLogitReplicas x (E + 1) words of 8 B, each copy padded to even
+  size_t ll_act = 0;      // kActReplicas x (k*I + Is) words, each copy padded to even
   // router for T tokens
   size_t r_logits = 0;    // [T, E + 1] fp32 (column E: shared-gate logit)
   // grouped path (T > 1)
