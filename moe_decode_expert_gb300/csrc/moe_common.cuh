@@ -146,8 +146,10 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
-__device__ __forceinline__ float sigmoid_f(float s) { return 1.0f / (1.0f + expf(-s)); }
+// g * sigmoid(g) and sigmoid(s) with a correctly rounded reciprocal (no
+// division slow path); expf keeps full fp32 accuracy.
+__device__ __forceinline__ float silu_f(float g) { return g * __frcp_rn(1.0f + expf(-g)); }
+__device__ __forceinline__ float sigmoid_f(float s) { return __frcp_rn(1.0f + expf(-s)); }
 
 // Order-preserving map of a finite fp32 onto uint32 (larger float -> larger
 // key).  Every finite value (and -inf) maps above 0, so 0 can mark "taken".

@@ -57,7 +57,7 @@ struct DecodeArgs {
   int ll_stride;   // words between the copies of the logit words
   int act_stride;  // words between the copies of the activation words
   uint32_t rs_r, rs_s;  // shared-memory row strides (bytes) of the routed and shared W2 rows
-  uint32_t off_lg, off_act, off_terms, off_w2;
+  uint32_t off_xh, off_lg, off_act, off_terms, off_w2;
   uint64_t timeout_ns;
 };
 
@@ -175,6 +175,65 @@ __device__ __forceinline__ void cp_async16_pred(uint32_t dst, const void* src, b
 }
 
 
+// 16-byte shared load, or zeros without a load when `pred` is false.
+__device__ __forceinline__ uint4 lds128_pred(uint32_t addr, bool pred) {
+  uint4 r;
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %5, 0;\n\tmov.b32 %0, 0;\n\tmov.b32 %1, 0;\n\tmov.b32 %2, 0;\n\t"
+      "mov.b32 %3, 0;\n\t@q ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n\t}"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "r"(addr), "r"(static_cast<int>(pred)));
+  return r;
+}
+
+// ---- CTA GEMV on m16n8k16 steps, split by columns over the 8 warps.
+// Up to 16 rows per pass, all in one MMA tile: lane (g, t) streams 16-byte
+// chunks of rows g and g + 8 (columns c0 + 32jj + 8t .. +7, jj < 8, of the
+// warp's column slice) into registers, the A fragment of 16 rows x 16 columns
+// per k-step; x, in the storage type in shared memory, is column 0 of B.
+// Within a 16-byte chunk, elements 0-3 form one k-step and 4-7 the next, the
+// same columns on both sides.  Column 0 of D holds the 16 rows' partial dot
+// products (lanes with t = 0: rows g and g + 8).
+template <int DT>
+struct Gemv16 {
+  uint4 w[2][8];  // [rows g / g + 8][chunk]
+
+  __device__ __forceinline__ void issue(const uint8_t* r0, bool v0, const uint8_t* r1, bool v1, int c0, int cend,
+                                        int t) {
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+      const int c = c0 + 32 * jj + 8 * t;
+      const bool in = c < cend;
+      const size_t off = 2 * static_cast<size_t>(in ? c : 0);
+      w[0][jj] = ld_stream16_pred(r0 + off, in && v0);
+      w[1][jj] = ld_stream16_pred(r1 + off, in && v1);
+    }
+  }
+
+  __device__ __forceinline__ void mma(uint32_t xh, int c0, int cend, int lane, float (&acc)[2][4]) const {
+    const int t = lane & 3;
+    const bool xl = lane < 4;  // B column 0 (n = lane / 4 = 0)
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+      const int c = c0 + 32 * jj + 8 * t;
+      const uint4 xv = lds128_pred(xh + 2 * static_cast<uint32_t>(c < cend ? c : 0), xl && c < cend);
+      mma16816<DT>(acc[jj & 1], w[0][jj].x, w[1][jj].x, w[0][jj].y, w[1][jj].y, xv.x, xv.y);
+      mma16816<DT>(acc[jj & 1], w[0][jj].z, w[1][jj].z, w[0][jj].w, w[1][jj].w, xv.z, xv.w);
+    }
+  }
+};
+
+// Lanes with t = 0 write the partial dot products of rows rg + g and
+// rg + g + 8 into part[warp][...].
+__device__ __forceinline__ void gemv_store_partials(float (*part)[64], int warp, int lane, int rg,
+                                                    const float (&acc)[2][4]) {
+  if ((lane & 3) == 0) {
+    const int g = lane >> 2;
+    part[warp][rg + g] = acc[0][0] + acc[1][0];
+    part[warp][rg + g + 8] = acc[0][2] + acc[1][2];
+  }
+}
+
 // v = t0 + t1 + t2 in the storage type: t0 = rn(v), t1 = rn(v - t0),
 // t2 = rn(v - t0 - t1) (both differences are exact in fp32): about 24
 // significant bits in bf16.  term[s] packs term s of v.x (low half) and v.y.
@@ -218,6 +277,7 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
   __shared__ float s_red[kDecWarps][64];
 
   float* xs = reinterpret_cast<float*>(smem);
+  uint16_t* xh = reinterpret_cast<uint16_t*>(smem + a.off_xh);  // x in its storage type
   float* lg = reinterpret_cast<float*>(smem + a.off_lg);
   float* acts = reinterpret_cast<float*>(smem + a.off_act);
   uint16_t* terms = reinterpret_cast<uint16_t*>(smem + a.off_terms);
@@ -289,36 +349,49 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
   pdl_launch_dependents();
   __syncthreads();
 
-  // ---- phase 1: routing-independent rows; the first round's loads go out
-  // before x is staged (and, with static weights, before the PDL wait)
-  const int n1 = E + a.has_gate + Is;
-  int q = warp;
-  int u = q * G + cta;
-  RowPair<DT> rp;
-  auto setup_unit = [&](int uu) {
-    if (uu < E) {
-      rp.r0 = a.wr + static_cast<size_t>(uu) * rowb; rp.r1 = rp.r0; rp.two = 0;
-    } else if (uu < E + a.has_gate) {
-      rp.r0 = a.swg; rp.r1 = rp.r0; rp.two = 0;
-    } else {
-      const int i = uu - E - a.has_gate;
-      rp.r0 = a.sw13 + static_cast<size_t>(i) * rowb;
-      rp.r1 = a.sw13 + static_cast<size_t>(Is + i) * rowb;
-      rp.two = 1;
-    }
+  // ---- phase 1: routing-independent rows of this CTA — its router rows
+  // u = cta + qG < E (and the shared gate row), then its shared-expert pairs
+  // (gate rows, then up rows) — as one CTA GEMV; the first pass's loads go out
+  // before x is staged (and, with static weights, before the PDL wait).
+  const int g = lane >> 2, t = lane & 3;
+  const int E1 = E + a.has_gate;
+  const int n1 = E1 + Is;
+  const int nL = cta < E1 ? (E1 - 1 - cta) / G + 1 : 0;  // logit rows
+  const int nU = cta < n1 ? (n1 - 1 - cta) / G + 1 : 0;
+  const int nS = nU - nL;                                  // shared pairs
+  const int R1 = nL + 2 * nS;                              // <= 64 (checked on the host)
+  auto p1_row = [&](int r, bool& valid) -> const uint8_t* {
+    valid = r < R1;
+    const int rr = r - nL;
+    const int pi = rr < nS ? rr : rr - nS;
+    const int uL = min(cta + r * G, E);
+    const int i = max(0, cta + (nL + pi) * G - E1);
+    const uint8_t* pl = uL < E ? a.wr + static_cast<size_t>(uL) * rowb : a.swg;
+    const uint8_t* ps = a.sw13 + static_cast<size_t>(rr < nS ? i : Is + i) * rowb;
+    return !valid ? a.wr : (r < nL ? pl : ps);
   };
+  const int cpw = ((H + 255) >> 8) * 32;  // columns per warp (H / 8, rounded up to 32)
+  const int c0w = min(warp * cpw, H), cendw = min(c0w + cpw, H);
+  const int cb1 = min(c0w + 256, cendw);  // end of the first 256-column batch
+  const uint32_t xha = smem_u32(xh);
+  Gemv16<DT> gv;
+  bool va, vb;
+  const uint8_t* ra = p1_row(g, va);
+  const uint8_t* rb = p1_row(g + 8, vb);
   if (a.static_weights) {
-    if (u < n1) { setup_unit(u); rp.issue(0, nch, lane); }
+    gv.issue(ra, va, rb, vb, c0w, cb1, t);
     if (Is > 0) copy_w2_cols(true);
   }
   pdl_wait();  // x (and anything else an earlier kernel wrote) is visible from here
-  if (!a.static_weights && u < n1) { setup_unit(u); rp.issue(0, nch, lane); }
+  if (!a.static_weights) gv.issue(ra, va, rb, vb, c0w, cb1, t);
 
   uint32_t gen_prev = 0;
   if (tid == 0) gen_prev = ld_relaxed_u32(&a.ctrl->gen);  // in flight together with x
   for (int c = tid; c < nch; c += kDecThreads) {
+    const uint4 raw = ld_ordered16(a.x + 16 * static_cast<size_t>(c));
+    *reinterpret_cast<uint4*>(xh + 8 * c) = raw;
     float f[8];
-    unpack8<DT>(ld_ordered16(a.x + 16 * static_cast<size_t>(c)), f);
+    unpack8<DT>(raw, f);
     reinterpret_cast<float4*>(xs)[2 * c] = make_float4(f[0], f[1], f[2], f[3]);
     reinterpret_cast<float4*>(xs)[2 * c + 1] = make_float4(f[4], f[5], f[6], f[7]);
   }
@@ -333,20 +406,38 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
   __syncthreads();
   const uint32_t epoch = s_epoch;
 
-  // Every CTA reads all logits and every activation, so each word is
-  // published in several copies (readers spread over more L2 lines).
-  while (u < n1) {
-    float d0, d1;
-    rp.finish(xs, nch, lane, d0, d1);
-    if (u < E + a.has_gate) {
-      if (lane < kLogitReplicas) ll_store(a.ll_logits + static_cast<size_t>(lane) * a.ll_stride + u, d0, epoch);
-    } else if (lane < kActReplicas) {
-      ll_store(a.ll_act + static_cast<size_t>(lane) * a.act_stride + P + (u - E - a.has_gate), silu_f(d0) * d1,
-               epoch);
+  for (int rg = 0; rg < R1; rg += 16) {
+    float acc[2][4] = {};
+    for (int cb = c0w; cb < cendw; cb += 256) {
+      if (rg > 0 || cb > c0w) {
+        ra = p1_row(rg + g, va);
+        rb = p1_row(rg + 8 + g, vb);
+        gv.issue(ra, va, rb, vb, cb, min(cb + 256, cendw), t);
+      }
+      gv.mma(xha, cb, min(cb + 256, cendw), lane, acc);
     }
-    q += kDecWarps;
-    u = q * G + cta;
-    if (u < n1) { setup_unit(u); rp.issue(0, nch, lane); }
+    gemv_store_partials(s_red, warp, lane, rg, acc);
+  }
+  __syncthreads();
+  // Every CTA reads all logits and every activation, so each word is
+  // published in several copies (readers spread over more L2 lines):
+  // eight threads per result, one copy each.
+  for (int o = tid >> 3; o < nL + nS; o += kDecThreads / 8) {
+    const int rep = tid & 7;
+    const bool logit = o < nL;
+    const int pi = o - nL;
+    const int ra0 = logit ? o : nL + pi, rb0 = logit ? o : nL + nS + pi;  // the two rows combined
+    float gs = 0.0f, us = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kDecWarps; ++w) {
+      gs += s_red[w][ra0];
+      us += s_red[w][rb0];
+    }
+    const float v = logit ? gs : silu_f(gs) * us;
+    uint64_t* dst = logit ? a.ll_logits + static_cast<size_t>(rep) * a.ll_stride + cta + o * G
+                          : a.ll_act + static_cast<size_t>(rep & (kActReplicas - 1)) * a.act_stride + P +
+                                (cta + (nL + pi) * G - E1);
+    if (rep < (logit ? kLogitReplicas : kActReplicas)) ll_store(dst, v, epoch);
   }
 
   // ---- phase 2: the logits, their top-k (fp32, lower index first on ties)
@@ -380,7 +471,7 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
       const uint64_t kc = s_cand[c];
       int cnt = 0;
 #pragma unroll
-      for (int jj = 0; jj < 16; ++jj) cnt += s_cand[q4 * 16 + jj] > kc ? 1 : 0;
+      for (int jj = 0; jj < 16; ++jj) cnt += s_cand[4 * jj + q4] > kc ? 1 : 0;  // 4 adjacent words per load
       cnt += __shfl_xor_sync(0xffffffffu, cnt, 1);
       cnt += __shfl_xor_sync(0xffffffffu, cnt, 2);
       if (q4 == 0 && kc != 0ull && cnt < k) {
@@ -399,7 +490,8 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
   }
   __syncthreads();
   const bool ranked = s_fail == 0;  // uniform: read after the barrier
-  if (warp == 0) {
+  // warp 0: routing weights and the shared gate (then s_wready)
+  auto weights = [&]() {
     if (ranked) {
       warp_routing_weights(lg, E, s_sel, k, a.norm_topk, s_w);
       if (lane == 0) s_gate = a.has_gate ? sigmoid_f(lg[E]) : 1.0f;
@@ -413,7 +505,8 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
       __threadfence_block();
       s_wready = 1;
     }
-  }
+  };
+  if (DEPTH == 2 && warp == 0) weights();
 
   // ---- phase 3: this CTA's share of the k*I routed gate/up pairs.  Warps
   // take pairs in order from a shared counter, so warp 0 (busy ranking) only
@@ -454,10 +547,50 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
     if (lane < kActReplicas) ll_store(a.ll_act + static_cast<size_t>(lane) * a.act_stride + p, silu_f(g) * up * s_w[r.j], epoch);
     return true;
   };
-  if (ranked && !s_fail) {
+  if constexpr (DEPTH == 1) {
+    // At most 8 pairs per CTA: all of them as one CTA GEMV (gate rows, then
+    // up rows), loads issued before the W2 copies and the routing weights.
+    if (ranked) {
+      const int np3 = cta < P ? (P - 1 - cta) / G + 1 : 0;
+      auto p3_row = [&](int r, bool& valid) -> const uint8_t* {
+        valid = r < 2 * np3;
+        const int pi = r < np3 ? r : r - np3;
+        const int p = pi * G + cta;
+        const int j = min(p / I, k - 1), i = p - j * I;
+        return a.w13 + (static_cast<size_t>(s_ids[j]) * 2 * I + (r < np3 ? i : I + i)) * rowb;
+      };
+      ra = p3_row(g, va);
+      rb = p3_row(g + 8, vb);
+      gv.issue(ra, va, rb, vb, c0w, cb1, t);
+      if (warp == 0) weights();
+      copy_w2_cols(false);
+      float acc[2][4] = {};
+      for (int cb = c0w; cb < cendw; cb += 256) {
+        if (cb > c0w) gv.issue(ra, va, rb, vb, cb, min(cb + 256, cendw), t);
+        gv.mma(xha, cb, min(cb + 256, cendw), lane, acc);
+      }
+      gemv_store_partials(s_red, warp, lane, 0, acc);
+      __syncthreads();
+      for (int o = tid >> 2; o < np3; o += kDecThreads / 4) {
+        const int rep = tid & 3;
+        float gs = 0.0f, us = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kDecWarps; ++w) {
+          gs += s_red[w][o];
+          us += s_red[w][np3 + o];
+        }
+        const int p = o * G + cta;
+        const int j = min(p / I, k - 1);
+        if (rep < kActReplicas)
+          ll_store(a.ll_act + static_cast<size_t>(rep) * a.act_stride + p, silu_f(gs) * us * s_w[j], epoch);
+      }
+    } else if (warp == 0) {
+      weights();
+    }
+  } else if (ranked && !s_fail) {
     bool copied = false;
-    if constexpr (DEPTH == 2) {
-      RowPair<DT> rq;
+    {
+      RowPair<DT> rp, rq;
       for (;;) {
         const int qq = grab(2);
         const int pa = qq * G + cta, pb = (qq + 1) * G + cta;
@@ -467,14 +600,6 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
         if (!copied) { copy_w2_cols(false); copied = true; }
         if (!end_pair(rp, pa) || pb >= P) break;
         if (!end_pair(rq, pb)) break;
-      }
-    } else {
-      for (;;) {
-        const int p = grab(1) * G + cta;
-        if (p >= P) break;
-        start_pair(rp, p);
-        if (!copied) { copy_w2_cols(false); copied = true; }
-        if (!end_pair(rp, p)) break;
       }
     }
     if (!copied) copy_w2_cols(false);
@@ -673,12 +798,14 @@ int decode_grid(const moe_cfg_t& c) {
 // (conflict-free ldmatrix).
 static uint32_t w2_row_stride(int n) { return static_cast<uint32_t>(((n / 8) | 1) * 16); }
 
-static void decode_smem_layout(const moe_cfg_t& c, int G, uint32_t& off_lg, uint32_t& off_act,
+static void decode_smem_layout(const moe_cfg_t& c, int G, uint32_t& off_xh, uint32_t& off_lg, uint32_t& off_act,
                                uint32_t& off_terms, uint32_t& off_w2, size_t& total) {
   const size_t H = c.hidden, E = c.n_experts, k = c.top_k, I = c.inter, Is = c.shared_inter;
   const size_t hn_max = (H + G - 1) / G;
   const size_t Kp = (k * I + Is + 15) / 16 * 16;
   size_t off = align_up(H * 4, 128);
+  off_xh = static_cast<uint32_t>(off);
+  off += align_up(H * 2, 128);
   off_lg = static_cast<uint32_t>(off);
   off += align_up((E + 2) * 4, 128);
   off_act = static_cast<uint32_t>(off);
@@ -691,9 +818,9 @@ static void decode_smem_layout(const moe_cfg_t& c, int G, uint32_t& off_lg, uint
 }
 
 size_t decode_smem_bytes(const moe_cfg_t& c, int G) {
-  uint32_t a, b, d, e;
+  uint32_t a, b, d, e, f;
   size_t t;
-  decode_smem_layout(c, G, a, b, d, e, t);
+  decode_smem_layout(c, G, a, b, d, e, f, t);
   return t;
 }
 
@@ -751,10 +878,12 @@ moe_status_t launch_decode_fused(const moe_cfg_t& c, const BlockPtrs& p, uint8_t
   a.rs_r = w2_row_stride(c.inter);
   a.rs_s = w2_row_stride(c.shared_inter);
   size_t smem;
-  decode_smem_layout(c, G, a.off_lg, a.off_act, a.off_terms, a.off_w2, smem);
+  decode_smem_layout(c, G, a.off_xh, a.off_lg, a.off_act, a.off_terms, a.off_w2, smem);
   a.timeout_ns = wait_timeout_ns();
   if (smem > 227 * 1024)
     return set_error(MOE_ERR_UNSUPPORTED, "decode: needs %zu B of shared memory per CTA (max 232448)", smem);
+  if (2 * ((c.n_experts + c.has_shared_gate + c.shared_inter + G - 1) / G) > 64)
+    return set_error(MOE_ERR_UNSUPPORTED, "decode: more than 64 routing-independent rows per CTA");
   if ((c.hidden + G - 1) / G > 64)
     return set_error(MOE_ERR_UNSUPPORTED, "decode: %d output rows per CTA (hidden / CTAs) exceed 64",
                      (c.hidden + G - 1) / G);
