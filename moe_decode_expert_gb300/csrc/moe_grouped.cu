@@ -35,6 +35,8 @@ __global__ void __launch_bounds__(1024) group_kernel(const int32_t* __restrict__
                                                      int has_shared, int32_t* counts_out,
                                                      int32_t* offsets, int32_t* perm, int32_t* tiles,
                                                      int write_tiles, Control* ctrl) {
+  pdl_launch_dependents();  // let the next kernel on the stream launch early
+  pdl_wait();               // inputs written by the previous kernel are visible
   __shared__ int32_t cnt[1025 + 1];
   __shared__ int32_t cur[1025 + 1];
   __shared__ int32_t tcnt[1025 + 1];
@@ -139,6 +141,8 @@ __global__ void __launch_bounds__(kGThreads) grouped_w13_kernel(
     const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets,
     const int32_t* __restrict__ perm, const int32_t* __restrict__ tiles, int T, int H, int E, int k,
     int I, int Is, int act_stride, float* __restrict__ act) {
+  pdl_launch_dependents();  // let the next kernel on the stream launch early
+  pdl_wait();               // inputs written by the previous kernel are visible
   extern __shared__ __align__(16) float xs[];   // [kTN][H] fp32
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tiles = counts[E + 1];
@@ -207,6 +211,8 @@ __global__ void __launch_bounds__(kGThreads) grouped_w2_kernel(
     const int32_t* __restrict__ tiles, const float* __restrict__ topk_w,
     const float* __restrict__ gate_logits, int gate_stride, int has_gate, int T, int H, int E, int k,
     int I, int Is, int act_stride, const float* __restrict__ act, float* __restrict__ y) {
+  pdl_launch_dependents();  // let the next kernel on the stream launch early
+  pdl_wait();               // inputs written by the previous kernel are visible
   extern __shared__ __align__(16) float as[];   // [kTN][Imax] fp32
   __shared__ float s_wt[kTN];
   __shared__ int s_pair[kTN];
@@ -268,6 +274,8 @@ __global__ void __launch_bounds__(kGThreads) grouped_w2_kernel(
 // ---------------------------------------------------------------- combine
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, int T, int H, int k,
                                                       int has_shared, void* out, int out_dtype) {
+  pdl_launch_dependents();  // let the next kernel on the stream launch early
+  pdl_wait();               // inputs written by the previous kernel are visible
   // grid (ceil(H/4 / 256), T): four consecutive outputs of token blockIdx.y per
   // thread (H % 8 == 0); the sum runs in slot order, then the shared part
   const int H4 = H >> 2;
@@ -316,7 +324,7 @@ moe_status_t launch_grouped(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws,
   const int Imax = I > Is ? I : Is;
 
   const bool use_tc = !(c.flags & MOE_FLAG_GROUPED_SIMT) && L.tc_n > 0 && tc_path_supported(c);
-  group_kernel<<<1, 1024, 0, st>>>(p.topk_ids, T, k, E, Is > 0, counts, offsets, perm, tiles, use_tc ? 0 : 1, ctrl);
+  launch_pdl(group_kernel, dim3(1), dim3(1024), 0, st, p.topk_ids, T, k, E, Is > 0, counts, offsets, perm, tiles, use_tc ? 0 : 1, ctrl);
   if (moe_status_t s = check_launch("group_kernel")) return s;
 
   const int sms = sm_count();
@@ -339,30 +347,30 @@ moe_status_t launch_grouped(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws,
     const uint8_t* x = static_cast<const uint8_t*>(p.x);
     if (c.dtype == MOE_BF16) {
       cudaFuncSetAttribute(grouped_w13_kernel<MOE_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem13);
-      grouped_w13_kernel<MOE_BF16><<<g13, kGThreads, smem13, st>>>(
+      launch_pdl(grouped_w13_kernel<MOE_BF16>, dim3(g13), dim3(kGThreads), smem13, st, 
           x, static_cast<const uint8_t*>(p.w13), static_cast<const uint8_t*>(p.shared_w13), counts, offsets,
           perm, tiles, T, H, E, k, I, Is, Imax, act);
     } else {
       cudaFuncSetAttribute(grouped_w13_kernel<MOE_F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem13);
-      grouped_w13_kernel<MOE_F16><<<g13, kGThreads, smem13, st>>>(
+      launch_pdl(grouped_w13_kernel<MOE_F16>, dim3(g13), dim3(kGThreads), smem13, st, 
           x, static_cast<const uint8_t*>(p.w13), static_cast<const uint8_t*>(p.shared_w13), counts, offsets,
           perm, tiles, T, H, E, k, I, Is, Imax, act);
     }
     if (moe_status_t s = check_launch("grouped_w13_kernel")) return s;
     if (c.dtype == MOE_BF16) {
       cudaFuncSetAttribute(grouped_w2_kernel<MOE_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
-      grouped_w2_kernel<MOE_BF16><<<g2, kGThreads, smem2, st>>>(
+      launch_pdl(grouped_w2_kernel<MOE_BF16>, dim3(g2), dim3(kGThreads), smem2, st, 
           static_cast<const uint8_t*>(p.w2), static_cast<const uint8_t*>(p.shared_w2), counts, offsets, perm,
           tiles, p.topk_w, glog, gate_stride, c.has_shared_gate, T, H, E, k, I, Is, Imax, act, y);
     } else {
       cudaFuncSetAttribute(grouped_w2_kernel<MOE_F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
-      grouped_w2_kernel<MOE_F16><<<g2, kGThreads, smem2, st>>>(
+      launch_pdl(grouped_w2_kernel<MOE_F16>, dim3(g2), dim3(kGThreads), smem2, st, 
           static_cast<const uint8_t*>(p.w2), static_cast<const uint8_t*>(p.shared_w2), counts, offsets, perm,
           tiles, p.topk_w, glog, gate_stride, c.has_shared_gate, T, H, E, k, I, Is, Imax, act, y);
     }
     if (moe_status_t s = check_launch("grouped_w2_kernel")) return s;
   }
-  combine_kernel<<<dim3((H / 4 + 255) / 256, T), 256, 0, st>>>(y, T, H, k, Is > 0, p.out, c.out_dtype);
+  launch_pdl(combine_kernel, dim3((H / 4 + 255) / 256, T), dim3(256), 0, st, y, T, H, k, Is > 0, p.out, c.out_dtype);
   if (moe_status_t s = check_launch("combine_kernel")) return s;
   stat_kernels(4);
   return MOE_OK;

@@ -160,6 +160,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                   const __grid_constant__ CUtensorMap mapB, const TcTile* __restrict__ tiles,
                   const int32_t* __restrict__ n_tiles_p, int H, int I, int Is, int E, int act_stride,
                   uint16_t* __restrict__ act_hi, uint16_t* __restrict__ act_lo, Control* ctrl, uint64_t timeout) {
+  pdl_launch_dependents();  // let the next kernel on the stream launch early
+  pdl_wait();               // inputs written by the previous kernel are visible
   constexpr uint32_t kStage = MT * kTileA + N * 128;
   constexpr int kStg = 128 * 17 * 4;
   constexpr int kStages = (kSmemBudget - kStg) / kStage > 8 ? 8 : (kSmemBudget - kStg) / kStage;
@@ -336,6 +338,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                  const int32_t* __restrict__ perm, const float* __restrict__ topk_w,
                  const float* __restrict__ gate_logits, int gate_stride, int has_gate, int T, int H, int I, int Is,
                  int E, int k, float* __restrict__ y, Control* ctrl, uint64_t timeout) {
+  pdl_launch_dependents();  // let the next kernel on the stream launch early
+  pdl_wait();               // inputs written by the previous kernel are visible
   constexpr uint32_t kStage = MT * kTileA + 2 * N * 128;
   constexpr int kStages = kSmemBudget / kStage > 8 ? 8 : kSmemBudget / kStage;
   constexpr uint32_t kCols = 2 * MT * N;
@@ -510,6 +514,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_router_kernel(const __grid_constant__ CUtensorMap mapWr, const __grid_constant__ CUtensorMap mapG,
                      const __grid_constant__ CUtensorMap mapX, int T, int H, int E, int E1, int mE, int nm,
                      float* __restrict__ logits, Control* ctrl, uint64_t timeout) {
+  pdl_launch_dependents();  // let the next kernel on the stream launch early
+  pdl_wait();               // inputs written by the previous kernel are visible
   constexpr uint32_t kStage = kTileA + N * 128;
   constexpr int kStages = kSmemBudget / kStage > 8 ? 8 : kSmemBudget / kStage;
   extern __shared__ uint8_t smem_raw[];
@@ -652,6 +658,8 @@ __global__ void __launch_bounds__(1024) tc_schedule_kernel(const int32_t* __rest
                                                            const int32_t* __restrict__ offsets, int E, int I,
                                                            int Is, int H, int N, int mt13, int mt2, int32_t* n13,
                                                            int32_t* n2, TcTile* t13, TcTile* t2) {
+  pdl_launch_dependents();  // let the next kernel on the stream launch early
+  pdl_wait();               // inputs written by the previous kernel are visible
   __shared__ unsigned long long wtot[32];
   __shared__ int pre13[1026], pre2[1026];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -719,6 +727,8 @@ __global__ void __launch_bounds__(1024) tc_schedule_kernel(const int32_t* __rest
 // up to 8 chunks per lane in flight.
 __global__ void __launch_bounds__(256) tc_gather_kernel(const uint8_t* __restrict__ x, const int32_t* __restrict__ perm,
                                                         int P, int T, int k, int H, uint8_t* __restrict__ xs) {
+  pdl_launch_dependents();  // let the next kernel on the stream launch early
+  pdl_wait();               // inputs written by the previous kernel are visible
   const int lane = threadIdx.x & 31;
   const int warps = gridDim.x * 8;
   const int nch = H >> 3;
@@ -815,11 +825,11 @@ static moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uin
   const int gate_stride = c.has_shared_gate ? E + 1 : E;
   const uint64_t timeout = wait_timeout_ns();
 
-  tc_schedule_kernel<<<1, 1024, 0, st>>>(counts, offsets, E, I, Is, H, N, kMT, kMT, sched, sched + 1, t13, t2);
+  launch_pdl(tc_schedule_kernel, dim3(1), dim3(1024), 0, st, counts, offsets, E, I, Is, H, N, kMT, kMT, sched, sched + 1, t13, t2);
   if (moe_status_t s = check_launch("tc_schedule_kernel")) return s;
   const int sms = sm_count();
   const int gg = (P + 7) / 8 < sms * 8 ? (P + 7) / 8 : sms * 8;
-  tc_gather_kernel<<<gg, 256, 0, st>>>(static_cast<const uint8_t*>(p.x), perm, P, T, k, H, xs);
+  launch_pdl(tc_gather_kernel, dim3(gg), dim3(256), 0, st, static_cast<const uint8_t*>(p.x), perm, P, T, k, H, xs);
   if (moe_status_t s = check_launch("tc_gather_kernel")) return s;
 
   CUtensorMap mA, mAs, mB, mW2, mW2s, mHi, mLo, mHiS, mLoS;
@@ -842,10 +852,10 @@ static moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uin
   cudaFuncSetAttribute(tc_w2_kernel<DT, N, kMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s2));
   const int g13 = static_cast<int>(L.tc_max13 < sms ? L.tc_max13 : sms);
   const int g2 = static_cast<int>(L.tc_max2 < sms ? L.tc_max2 : sms);
-  tc_w13_kernel<DT, N, kMT><<<g13 > 0 ? g13 : 1, kTcThreads, s13, st>>>(mA, mAs, mB, t13, sched, H, I, Is, E, Imax,
+  launch_pdl(tc_w13_kernel<DT, N, kMT>, dim3(g13 > 0 ? g13 : 1), dim3(kTcThreads), s13, st, mA, mAs, mB, t13, sched, H, I, Is, E, Imax,
                                                                        ahi, alo, ctrl, timeout);
   if (moe_status_t s = check_launch("tc_w13_kernel")) return s;
-  tc_w2_kernel<DT, N, kMT><<<g2 > 0 ? g2 : 1, kTcThreads, s2, st>>>(mW2, mW2s, mHi, mLo, mHiS, mLoS, t2, sched + 1,
+  launch_pdl(tc_w2_kernel<DT, N, kMT>, dim3(g2 > 0 ? g2 : 1), dim3(kTcThreads), s2, st, mW2, mW2s, mHi, mLo, mHiS, mLoS, t2, sched + 1,
                                                                    perm, p.topk_w, glog, gate_stride,
                                                                    c.has_shared_gate, T, H, I, Is, E, k, y, ctrl,
                                                                    timeout);
@@ -878,7 +888,7 @@ moe_status_t launch_tc_router(const moe_cfg_t& c, const void* x, const void* rou
   const int tiles = nm * ((T + N - 1) / N);
   const int sms = sm_count();
   const int g = tiles < sms ? tiles : sms;
-  tc_router_kernel<DT, N><<<g, kTcThreads, smem, st>>>(mWr, mG, mX, T, H, E, E1, mE, nm, logits, ctrl,
+  launch_pdl(tc_router_kernel<DT, N>, dim3(g), dim3(kTcThreads), smem, st, mWr, mG, mX, T, H, E, E1, mE, nm, logits, ctrl,
                                                        wait_timeout_ns());
   if (moe_status_t s = check_launch("tc_router_kernel")) return s;
   stat_kernels(1);

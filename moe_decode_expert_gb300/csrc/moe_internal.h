@@ -100,6 +100,26 @@ moe_status_t launch_tc_router(const moe_cfg_t& c, const void* x, const void* rou
 moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws, const WsLayout& L, int32_t T,
                               cudaStream_t st);
 
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while the previous kernel on the stream drains.  Every kernel of the library
+// runs griddepcontrol.wait before touching memory, so ordering is unchanged;
+// only the launch latency overlaps.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Grid size of the single-launch decode kernel for cfg c.
 int decode_grid(const moe_cfg_t& c);
 // Dynamic shared memory of that kernel (bytes) for grid G.

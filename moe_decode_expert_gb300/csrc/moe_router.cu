@@ -26,6 +26,8 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const uint8_t* __res
                                                             const uint8_t* __restrict__ wr,
                                                             const uint8_t* __restrict__ swg, int T,
                                                             int H, int E, int E1, float* __restrict__ logits) {
+  pdl_launch_dependents();  // let the next kernel on the stream launch early
+  pdl_wait();               // inputs written by the previous kernel are visible
   __shared__ float As[kRBK][kRBM + 4];   // router rows, k-major
   __shared__ float Bs[kRBK][kRBN + 4];   // tokens, k-major
   const int tid = threadIdx.x;
@@ -85,6 +87,8 @@ __global__ void __launch_bounds__(256) router_gemv_kernel(const uint8_t* __restr
                                                           const uint8_t* __restrict__ wr,
                                                           const uint8_t* __restrict__ swg, int T, int H, int E,
                                                           int E1, float* __restrict__ logits) {
+  pdl_launch_dependents();  // let the next kernel on the stream launch early
+  pdl_wait();               // inputs written by the previous kernel are visible
   extern __shared__ __align__(16) float xt[];  // [kGvTok][min(H, 2048)] fp32
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x * 8 + warp;
@@ -168,6 +172,8 @@ template <int MAXM>
 __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restrict__ logits, int T, int E,
                                                           int E1, int k, int norm_topk, int32_t* ids,
                                                           float* w, float* logits_out) {
+  pdl_launch_dependents();  // let the next kernel on the stream launch early
+  pdl_wait();               // inputs written by the previous kernel are visible
   __shared__ int s_ids[8][32];
   __shared__ float s_sel[8][32];
   __shared__ float s_w[8][32];
@@ -208,25 +214,25 @@ moe_status_t launch_router(const moe_cfg_t& c, const void* x, const void* router
     const size_t sm = static_cast<size_t>(kGvTok) * 2048 * 4;
     if (c.dtype == MOE_BF16) {
       cudaFuncSetAttribute(router_gemv_kernel<MOE_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-      router_gemv_kernel<MOE_BF16><<<gg, 256, sm, st>>>(xb, wb, swg, T, c.hidden, E, stride, lg);
+      launch_pdl(router_gemv_kernel<MOE_BF16>, dim3(gg), dim3(256), sm, st, xb, wb, swg, T, c.hidden, E, stride, lg);
     } else {
       cudaFuncSetAttribute(router_gemv_kernel<MOE_F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-      router_gemv_kernel<MOE_F16><<<gg, 256, sm, st>>>(xb, wb, swg, T, c.hidden, E, stride, lg);
+      launch_pdl(router_gemv_kernel<MOE_F16>, dim3(gg), dim3(256), sm, st, xb, wb, swg, T, c.hidden, E, stride, lg);
     }
   } else {
     dim3 g1((E1 + kRBM - 1) / kRBM, (T + kRBN - 1) / kRBN);
     if (c.dtype == MOE_BF16)
-      router_logits_kernel<MOE_BF16><<<g1, 256, 0, st>>>(xb, wb, swg, T, c.hidden, E, stride, lg);
+      launch_pdl(router_logits_kernel<MOE_BF16>, dim3(g1), dim3(256), 0, st, xb, wb, swg, T, c.hidden, E, stride, lg);
     else
-      router_logits_kernel<MOE_F16><<<g1, 256, 0, st>>>(xb, wb, swg, T, c.hidden, E, stride, lg);
+      launch_pdl(router_logits_kernel<MOE_F16>, dim3(g1), dim3(256), 0, st, xb, wb, swg, T, c.hidden, E, stride, lg);
   }
   if (moe_status_t s = check_launch("router_logits_kernel")) return s;
   // The logits rows are laid out with stride E1 only when the gate column exists.
   dim3 g2((T + 7) / 8);
   if (E <= 256)
-    router_topk_kernel<8><<<g2, 256, 0, st>>>(lg, T, E, stride, c.top_k, c.norm_topk, ids, w, logits_out);
+    launch_pdl(router_topk_kernel<8>, dim3(g2), dim3(256), 0, st, lg, T, E, stride, c.top_k, c.norm_topk, ids, w, logits_out);
   else
-    router_topk_kernel<32><<<g2, 256, 0, st>>>(lg, T, E, stride, c.top_k, c.norm_topk, ids, w, logits_out);
+    launch_pdl(router_topk_kernel<32>, dim3(g2), dim3(256), 0, st, lg, T, E, stride, c.top_k, c.norm_topk, ids, w, logits_out);
   if (moe_status_t s = check_launch("router_topk_kernel")) return s;
   stat_kernels(2);
   return MOE_OK;
