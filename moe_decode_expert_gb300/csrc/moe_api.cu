@@ -68,6 +68,8 @@ WsLayout ws_layout(const moe_cfg_t& c, int32_t T) {
   off = align_up(off + kActReplicas * ((k * I + Is + 1) & ~int64_t(1)) * 8, kWsAlign);
   L.r_logits = off;
   off = align_up(off + static_cast<size_t>(T) * (E + 1) * 4, kWsAlign);
+  L.r_part = off;
+  if (T <= 64) off = align_up(off + static_cast<size_t>(H / 256 + 1) * T * (E + 1) * 4, kWsAlign);
   if (T > 1) {
     const int64_t P = T * k + (Is > 0 ? T : 0);
     const int64_t tn = 8;  // pairs per tile of the grouped kernels

@@ -26,6 +26,7 @@ struct WsLayout {
   size_t ll_act = 0;      // kActReplicas x (k*I + Is) words, each copy padded to even
   // router for T tokens
   size_t r_logits = 0;    // [T, E + 1] fp32 (column E: shared-gate logit)
+  size_t r_part = 0;      // T <= 64: [H / 256 + 1, T, E + 1] fp32 split partial logits
   // grouped path (T > 1)
   size_t g_counts = 0;    // (E + 2) int32: tokens per expert (E = shared)
   size_t g_offsets = 0;   // (E + 2) int32: exclusive prefix of counts

@@ -167,11 +167,84 @@ __global__ void __launch_bounds__(256) router_gemv_kernel(const uint8_t* __restr
   }
 }
 
+// ---- small-T router on m16n8k16 tensor-core steps
+// logits[t, e] for T <= 64 tokens and E + gate <= 257 rows: 16 router rows
+// (the gate vector as row E) are the A operand, the tokens (8 per n-tile) the
+// B columns.  CTA (m-tile, split s) takes columns [s*cpc, (s+1)*cpc) of H, its
+// 8 warps 32-column chunks of that range; lane (g, t) streams 16-byte chunks
+// of rows g and g + 8 and of token g (elements 0-3 of a chunk form one k-step,
+// 4-7 the next, the same on both sides).  The warps' sums meet in shared
+// memory and the CTA writes partial logits part[s][t][e]; the top-k kernel
+// adds the splits in order.
+template <int DT>
+__global__ void __launch_bounds__(256) router_mma_kernel(const uint8_t* __restrict__ x,
+                                                         const uint8_t* __restrict__ wr,
+                                                         const uint8_t* __restrict__ swg, int T, int H, int E,
+                                                         int E1, int cpc, float* __restrict__ part) {
+  pdl_launch_dependents();  // let the next kernel on the stream launch early
+  pdl_wait();               // inputs written by the previous kernel are visible
+  __shared__ float red[8][16][64];  // [warp][row][token]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+  const int m0 = blockIdx.x * 16, s = blockIdx.y;
+  const int c0 = s * cpc, c1 = min(c0 + cpc, H);
+  const size_t rowb = static_cast<size_t>(H) * 2;
+  auto rowp = [&](int r) -> const uint8_t* {  // rows past E1 repeat the last row (discarded)
+    const int e = min(m0 + r, E1 - 1);
+    return e < E ? wr + static_cast<size_t>(e) * rowb : swg;
+  };
+  const uint8_t* ra = rowp(g);
+  const uint8_t* rb = rowp(g + 8);
+  const int nT = (T + 7) >> 3;
+  float acc[8][4];
+#pragma unroll
+  for (int n = 0; n < 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.0f;
+  for (int cc = c0 + 32 * warp; cc < c1; cc += 256) {
+    const bool cin = cc + 8 * t < c1;
+    const int c = cin ? cc + 8 * t : c1 - 8;  // clamped: its B entries are zeroed
+    const uint4 wa = ld_nc16(ra + 2 * static_cast<size_t>(c));
+    const uint4 wb = ld_nc16(rb + 2 * static_cast<size_t>(c));
+#pragma unroll
+    for (int n = 0; n < 8; ++n) {
+      if (n < nT) {
+        const int tok = min(n * 8 + g, T - 1);  // tokens past T repeat the last (discarded)
+        uint4 xv = ld_nc16(x + (static_cast<size_t>(tok) * H + c) * 2);
+        xv = cin ? xv : make_uint4(0u, 0u, 0u, 0u);
+        mma16816<DT>(acc[n], wa.x, wb.x, wa.y, wb.y, xv.x, xv.y);
+        mma16816<DT>(acc[n], wa.z, wb.z, wa.w, wb.w, xv.z, xv.w);
+      }
+    }
+  }
+  // D fragment: rows g / g + 8, tokens n*8 + 2t, 2t + 1
+#pragma unroll
+  for (int n = 0; n < 8; ++n) {
+    if (n < nT) {
+      red[warp][g][n * 8 + 2 * t] = acc[n][0];
+      red[warp][g][n * 8 + 2 * t + 1] = acc[n][1];
+      red[warp][g + 8][n * 8 + 2 * t] = acc[n][2];
+      red[warp][g + 8][n * 8 + 2 * t + 1] = acc[n][3];
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < 16 * 64; i += 256) {
+    const int r = i >> 6, tt = i & 63;
+    const int e = m0 + r;
+    if (tt < T && e < E1) {
+      float v = 0.0f;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) v += red[w][r][tt];
+      part[(static_cast<size_t>(s) * T + tt) * E1 + e] = v;
+    }
+  }
+}
+
 // One warp per token: rank, weights, outputs.
+// With nsplit > 0 the logits arrive as nsplit partial sums part[s][t][e]
+// (router_mma_kernel): they are added in split order, stored into `logits`
+// (the [T, E1] buffer later kernels read) and ranked from shared memory.
 template <int MAXM>
-__global__ void __launch_bounds__(256) router_topk_kernel(const float* __restrict__ logits, int T, int E,
-                                                          int E1, int k, int norm_topk, int32_t* ids,
-                                                          float* w, float* logits_out) {
+__global__ void __launch_bounds__(256) router_topk_kernel(float* __restrict__ logits, const float* __restrict__ part,
+                                                          int nsplit, int T, int E, int E1, int k, int norm_topk,
+                                                          int32_t* ids, float* w, float* logits_out) {
   pdl_launch_dependents();  // let the next kernel on the stream launch early
   pdl_wait();               // inputs written by the previous kernel are visible
   __shared__ int s_ids[8][32];
@@ -180,7 +253,20 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
+  __shared__ float s_row[8][MAXM == 8 ? 258 : 1];
   const float* row = logits + static_cast<size_t>(t) * E1;
+  if constexpr (MAXM == 8) {
+    if (nsplit > 0) {
+      for (int e = lane; e < E1; e += 32) {
+        float v = 0.0f;
+        for (int sp = 0; sp < nsplit; ++sp) v += part[(static_cast<size_t>(sp) * T + t) * E1 + e];
+        s_row[warp][e] = v;
+        logits[static_cast<size_t>(t) * E1 + e] = v;
+      }
+      __syncwarp();
+      row = s_row[warp];
+    }
+  }
   if constexpr (MAXM == 8) warp_topk_sorted8(row, E, k, s_ids[warp], s_sel[warp]);
   else warp_topk<MAXM>(row, E, k, s_ids[warp], s_sel[warp]);
   __syncwarp();
@@ -205,10 +291,25 @@ moe_status_t launch_router(const moe_cfg_t& c, const void* x, const void* router
   const uint8_t* xb = static_cast<const uint8_t*>(x);
   const uint8_t* wb = static_cast<const uint8_t*>(router_w);
   const bool tc = T >= kRouterTcMinT && tc_router_supported(c);
+  int nsplit = 0;  // > 0: the logits are split partial sums (router_mma_kernel)
   if (tc) {
     if (moe_status_t s = launch_tc_router(c, x, router_w, swg, T, lg, stride,
                                           reinterpret_cast<Control*>(ws + L.ctrl), st))
       return s;
+  } else if (T <= kRouterGemvMaxT && E1 <= 257 && c.hidden % 8 == 0) {
+    const int nm = (stride + 15) / 16;
+    int S = c.hidden / 256;
+    const int smax = sm_count() / nm;
+    if (S > smax) S = smax;
+    if (S < 1) S = 1;
+    const int cpc = ((c.hidden + S - 1) / S + 31) / 32 * 32;
+    S = (c.hidden + cpc - 1) / cpc;
+    float* part = reinterpret_cast<float*>(ws + L.r_part);
+    if (c.dtype == MOE_BF16)
+      launch_pdl(router_mma_kernel<MOE_BF16>, dim3(nm, S), dim3(256), 0, st, xb, wb, swg, T, c.hidden, E, stride, cpc, part);
+    else
+      launch_pdl(router_mma_kernel<MOE_F16>, dim3(nm, S), dim3(256), 0, st, xb, wb, swg, T, c.hidden, E, stride, cpc, part);
+    nsplit = S;
   } else if (T <= kRouterGemvMaxT) {
     dim3 gg((E1 + 7) / 8, (T + kGvTok - 1) / kGvTok);
     const size_t sm = static_cast<size_t>(kGvTok) * 2048 * 4;
@@ -230,9 +331,9 @@ moe_status_t launch_router(const moe_cfg_t& c, const void* x, const void* router
   // The logits rows are laid out with stride E1 only when the gate column exists.
   dim3 g2((T + 7) / 8);
   if (E <= 256)
-    launch_pdl(router_topk_kernel<8>, dim3(g2), dim3(256), 0, st, lg, T, E, stride, c.top_k, c.norm_topk, ids, w, logits_out);
+    launch_pdl(router_topk_kernel<8>, dim3(g2), dim3(256), 0, st, lg, reinterpret_cast<const float*>(ws + L.r_part), nsplit, T, E, stride, c.top_k, c.norm_topk, ids, w, logits_out);
   else
-    launch_pdl(router_topk_kernel<32>, dim3(g2), dim3(256), 0, st, lg, T, E, stride, c.top_k, c.norm_topk, ids, w, logits_out);
+    launch_pdl(router_topk_kernel<32>, dim3(g2), dim3(256), 0, st, lg, static_cast<const float*>(nullptr), 0, T, E, stride, c.top_k, c.norm_topk, ids, w, logits_out);
   if (moe_status_t s = check_launch("router_topk_kernel")) return s;
   stat_kernels(2);
   return MOE_OK;
