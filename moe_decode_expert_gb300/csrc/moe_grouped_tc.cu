@@ -825,7 +825,13 @@ static moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uin
   const int gate_stride = c.has_shared_gate ? E + 1 : E;
   const uint64_t timeout = wait_timeout_ns();
 
-  launch_pdl(tc_schedule_kernel, dim3(1), dim3(1024), 0, st, counts, offsets, E, I, Is, H, N, kMT, kMT, sched, sched + 1, t13, t2);
+  // M-tiles per W13 tile: two share every token stage (half the token
+  // traffic), but when the pairs are few that leaves SMs idle, so a single
+  // M-tile per CTA then spreads the weight stream over twice the SMs.
+  const int sms0 = sm_count();
+  const int est13 = (T * k < E ? T * k : E) * ((I / 64 + kMT - 1) / kMT);  // W13 tiles with kMT
+  const int mt13 = 2 * est13 <= sms0 ? 1 : kMT;
+  launch_pdl(tc_schedule_kernel, dim3(1), dim3(1024), 0, st, counts, offsets, E, I, Is, H, N, mt13, kMT, sched, sched + 1, t13, t2);
   if (moe_status_t s = check_launch("tc_schedule_kernel")) return s;
   const int sms = sm_count();
   const int gg = (P + 7) / 8 < sms * 8 ? (P + 7) / 8 : sms * 8;
@@ -847,13 +853,21 @@ static moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uin
             make_map(&mLoS, DT, alo, IsM, P, static_cast<uint64_t>(Imax) * 2, N);
   if (!ok) return set_error(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
 
-  const size_t s13 = tc_smem13<N, kMT>(), s2 = tc_smem2<N, kMT>();
-  cudaFuncSetAttribute(tc_w13_kernel<DT, N, kMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s13));
+  const size_t s2 = tc_smem2<N, kMT>();
   cudaFuncSetAttribute(tc_w2_kernel<DT, N, kMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s2));
   const int g13 = static_cast<int>(L.tc_max13 < sms ? L.tc_max13 : sms);
   const int g2 = static_cast<int>(L.tc_max2 < sms ? L.tc_max2 : sms);
-  launch_pdl(tc_w13_kernel<DT, N, kMT>, dim3(g13 > 0 ? g13 : 1), dim3(kTcThreads), s13, st, mA, mAs, mB, t13, sched, H, I, Is, E, Imax,
-                                                                       ahi, alo, ctrl, timeout);
+  if (mt13 == 1) {
+    const size_t s13 = tc_smem13<N, 1>();
+    cudaFuncSetAttribute(tc_w13_kernel<DT, N, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s13));
+    launch_pdl(tc_w13_kernel<DT, N, 1>, dim3(g13 > 0 ? g13 : 1), dim3(kTcThreads), s13, st, mA, mAs, mB, t13, sched, H,
+               I, Is, E, Imax, ahi, alo, ctrl, timeout);
+  } else {
+    const size_t s13 = tc_smem13<N, kMT>();
+    cudaFuncSetAttribute(tc_w13_kernel<DT, N, kMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s13));
+    launch_pdl(tc_w13_kernel<DT, N, kMT>, dim3(g13 > 0 ? g13 : 1), dim3(kTcThreads), s13, st, mA, mAs, mB, t13, sched,
+               H, I, Is, E, Imax, ahi, alo, ctrl, timeout);
+  }
   if (moe_status_t s = check_launch("tc_w13_kernel")) return s;
   launch_pdl(tc_w2_kernel<DT, N, kMT>, dim3(g2 > 0 ? g2 : 1), dim3(kTcThreads), s2, st, mW2, mW2s, mHi, mLo, mHiS, mLoS, t2, sched + 1,
                                                                    perm, p.topk_w, glog, gate_stride,
