@@ -20,10 +20,10 @@
 
 #include "moe_common.cuh"
 #include "moe_internal.h"
+#include "moe_stages.cuh"
 
 namespace moe {
 
-constexpr int kTN = 8;            // pairs (tokens) per tile
 constexpr int kGThreads = 256;
 constexpr int kGWarps = kGThreads / 32;
 constexpr int kPB = 32;           // gate/up pairs per w13 work item
@@ -37,98 +37,7 @@ __global__ void __launch_bounds__(1024) group_kernel(const int32_t* __restrict__
                                                      int write_tiles, Control* ctrl) {
   pdl_launch_dependents();  // let the next kernel on the stream launch early
   pdl_wait();               // inputs written by the previous kernel are visible
-  __shared__ int32_t cnt[1025 + 1];
-  __shared__ int32_t cur[1025 + 1];
-  __shared__ int32_t tcnt[1025 + 1];
-  __shared__ int32_t wsum[32];
-  const int tid = threadIdx.x;
-  const int n = E + 1;  // experts + the shared expert
-  for (int e = tid; e < n; e += 1024) cnt[e] = 0;
-  __syncthreads();
-  const int np = T * k;
-  for (int base = tid; base < np; base += 1024 * 8) {  // 8 id loads in flight per thread
-    int ev[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) ev[u] = base + 1024 * u < np ? ids[base + 1024 * u] : -2;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int e = ev[u];
-      if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
-      else if (e != -2) report_error(ctrl, kDevBadExpert, static_cast<uint32_t>(base + 1024 * u));
-    }
-  }
-  if (tid == 0) cnt[E] = has_shared ? T : 0;
-  __syncthreads();
-
-  // Exclusive scans of pair counts and tile counts (two elements per thread at most).
-  const int lane = tid & 31, warp = tid >> 5;
-  int c0 = 0, c1 = 0, t0 = 0, t1 = 0;
-  const int e0 = 2 * tid, e1 = 2 * tid + 1;
-  if (e0 < n) { c0 = cnt[e0]; t0 = (c0 + kTN - 1) / kTN; }
-  if (e1 < n) { c1 = cnt[e1]; t1 = (c1 + kTN - 1) / kTN; }
-  // pack pair and tile sums into one 64-bit scan value
-  unsigned long long v = (static_cast<unsigned long long>(c0 + c1) << 32) | static_cast<unsigned>(t0 + t1);
-  unsigned long long incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  __shared__ unsigned long long wtot[32];
-  if (lane == 31) wtot[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    unsigned long long s = wtot[lane];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const unsigned long long y = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += y;
-    }
-    wtot[lane] = s;  // inclusive over warps
-  }
-  __syncthreads();
-  const unsigned long long before = incl - v + (warp ? wtot[warp - 1] : 0ull);
-  const int pb = static_cast<int>(before >> 32), tb = static_cast<int>(before & 0xffffffffu);
-  if (e0 < n) { cur[e0] = pb; tcnt[e0] = tb; }
-  if (e1 < n) { cur[e1] = pb + c0; tcnt[e1] = tb + t0; }
-  __syncthreads();
-  (void)wsum;
-  for (int e = tid; e < n; e += 1024) {
-    offsets[e] = cur[e];
-    counts_out[e] = cnt[e];
-  }
-  const unsigned long long tot = wtot[31];
-  const int n_tiles = static_cast<int>(tot & 0xffffffffu);
-  if (tid == 0) {
-    offsets[n] = static_cast<int>(tot >> 32);
-    counts_out[n] = n_tiles;  // number of tiles
-  }
-  if (write_tiles) {
-    // tile i belongs to the last expert whose first tile index is <= i
-    for (int i = tid; i < n_tiles; i += 1024) {
-      int lo = 0, hi = n - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (tcnt[mid] <= i) lo = mid; else hi = mid - 1;
-      }
-      tiles[2 * i] = lo;
-      tiles[2 * i + 1] = cur[lo] + (i - tcnt[lo]) * kTN;
-    }
-  }
-  __syncthreads();
-  // File routed pairs (any order within an expert) and the shared pairs (in token order).
-  for (int base = tid; base < np; base += 1024 * 8) {
-    int ev[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) ev[u] = base + 1024 * u < np ? ids[base + 1024 * u] : -2;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int e = ev[u];
-      if (e >= 0 && e < E) perm[atomicAdd(&cur[e], 1)] = base + 1024 * u;
-    }
-  }
-  if (has_shared)
-    for (int t = tid; t < T; t += 1024) perm[cur[E] + t] = np + t;
+  group_stage(ids, T, k, E, has_shared, counts_out, offsets, perm, tiles, write_tiles, ctrl);
 }
 
 // Token of pair p (routed pairs t*k + j, then shared pairs T*k + t).
@@ -310,8 +219,13 @@ moe_status_t launch_grouped(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws,
                             int32_t T, cudaStream_t st) {
   const int H = c.hidden, E = c.n_experts, k = c.top_k, I = c.inter, Is = c.shared_inter;
   Control* ctrl = reinterpret_cast<Control*>(ws + L.ctrl);
+  const bool use_tc = !(c.flags & MOE_FLAG_GROUPED_SIMT) && L.tc_n > 0 && tc_path_supported(c);
+  // very small batches on the tensor-core path: ranking, grouping and tile lists
+  // in one single-CTA launch (from T = 16 on the multi-CTA ranking is faster)
+  const bool fused = use_tc && T <= 8 && E <= 256;
+  int nsplit = -1;
   if (moe_status_t s = launch_router(c, p.x, p.router_w, p.shared_gate_w, T, p.topk_ids, p.topk_w,
-                                     nullptr, ws, L, st))
+                                     nullptr, ws, L, st, fused ? &nsplit : nullptr))
     return s;
   int32_t* counts = reinterpret_cast<int32_t*>(ws + L.g_counts);
   int32_t* offsets = reinterpret_cast<int32_t*>(ws + L.g_offsets);
@@ -323,16 +237,19 @@ moe_status_t launch_grouped(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws,
   const int gate_stride = c.has_shared_gate ? E + 1 : E;
   const int Imax = I > Is ? I : Is;
 
-  const bool use_tc = !(c.flags & MOE_FLAG_GROUPED_SIMT) && L.tc_n > 0 && tc_path_supported(c);
-  launch_pdl(group_kernel, dim3(1), dim3(1024), 0, st, p.topk_ids, T, k, E, Is > 0, counts, offsets, perm, tiles, use_tc ? 0 : 1, ctrl);
-  if (moe_status_t s = check_launch("group_kernel")) return s;
+  if (!fused) {
+    launch_pdl(group_kernel, dim3(1), dim3(1024), 0, st, p.topk_ids, T, k, E, Is > 0, counts, offsets, perm, tiles,
+               use_tc ? 0 : 1, ctrl);
+    if (moe_status_t s = check_launch("group_kernel")) return s;
+    stat_kernels(1);
+  }
 
   const int sms = sm_count();
   if ((c.flags & MOE_FLAG_GROUPED_TC) && !use_tc)
     return set_error(MOE_ERR_UNSUPPORTED, "grouped: the tensor-core path needs bf16, H %% 128 == 0, "
                                           "I and Is multiples of 64 and the TMA encoder");
   if (use_tc) {
-    if (moe_status_t s = launch_tc_passes(c, p, ws, L, T, st)) return s;
+    if (moe_status_t s = launch_tc_passes(c, p, ws, L, T, fused ? nsplit : -1, st)) return s;
     stat_grouped_tc();
   } else {
     const size_t smem13 = static_cast<size_t>(kTN) * H * 4;
@@ -369,10 +286,11 @@ moe_status_t launch_grouped(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws,
           tiles, p.topk_w, glog, gate_stride, c.has_shared_gate, T, H, E, k, I, Is, Imax, act, y);
     }
     if (moe_status_t s = check_launch("grouped_w2_kernel")) return s;
+    stat_kernels(2);
   }
   launch_pdl(combine_kernel, dim3((H / 4 + 255) / 256, T), dim3(256), 0, st, y, T, H, k, Is > 0, p.out, c.out_dtype);
   if (moe_status_t s = check_launch("combine_kernel")) return s;
-  stat_kernels(4);
+  stat_kernels(1);
   return MOE_OK;
 }
 

@@ -30,6 +30,7 @@
 
 #include "moe_common.cuh"
 #include "moe_internal.h"
+#include "moe_stages.cuh"
 
 namespace moe {
 
@@ -38,12 +39,6 @@ constexpr int kBK = 64;                 // K elements per stage: one 128-byte sw
 constexpr uint32_t kTileA = 128 * 128;  // 128 rows x 128 bytes
 constexpr int kSmemBudget = 220 * 1024;
 
-struct TcTile {
-  int32_t e;     // expert id, E = shared expert
-  int32_t m;     // M-tile index within the expert
-  int32_t pos0;  // first sorted pair position of the N-tile
-  int32_t n;     // valid tokens in the tile
-};
 
 // ----------------------------------------------------------------- PTX
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {
@@ -660,67 +655,35 @@ __global__ void __launch_bounds__(1024) tc_schedule_kernel(const int32_t* __rest
                                                            int32_t* n2, TcTile* t13, TcTile* t2) {
   pdl_launch_dependents();  // let the next kernel on the stream launch early
   pdl_wait();               // inputs written by the previous kernel are visible
-  __shared__ unsigned long long wtot[32];
-  __shared__ int pre13[1026], pre2[1026];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int n = E + 1;
-  // tiles of each expert (two experts per thread; n <= 1025)
-  int a13[2] = {0, 0}, a2[2] = {0, 0};
-  for (int s = 0; s < 2; ++s) {
-    const int e = 2 * tid + s;
-    if (e < n) {
-      const int cnt = counts[e];
-      const int ie = e == E ? Is : I;
-      const int nt = (cnt + N - 1) / N;
-      a13[s] = ie > 0 ? nt * ((ie / 64 + mt13 - 1) / mt13) : 0;
-      a2[s] = ie > 0 ? nt * ((H / 128 + mt2 - 1) / mt2) : 0;
-    }
-  }
-  unsigned long long v = (static_cast<unsigned long long>(a13[0] + a13[1]) << 32) | static_cast<unsigned>(a2[0] + a2[1]);
-  unsigned long long incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const unsigned long long yv = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += yv;
-  }
-  if (lane == 31) wtot[warp] = incl;
+  schedule_stage(counts, offsets, E, I, Is, H, N, mt13, mt2, n13, n2, t13, t2);
+}
+
+// Very small batches (T <= 8, E <= 256): the ranking of every token, the counting
+// sort of the pairs by expert and the tile lists of both tensor-core passes in
+// one single-CTA launch instead of three (each of those kernels is a few µs of
+// mostly fixed latency at this size).  Warps 0-15 rank the tokens, then all
+// 1024 threads group and schedule.
+__global__ void __launch_bounds__(1024) route_group_kernel(float* __restrict__ logits, const float* __restrict__ part,
+                                                           int nsplit, int T, int E, int E1, int k, int norm_topk,
+                                                           int32_t* ids, float* w, int has_shared, int32_t* counts,
+                                                           int32_t* offsets, int32_t* perm, Control* ctrl, int I,
+                                                           int Is, int H, int N, int mt13, int mt2, int32_t* n13,
+                                                           int32_t* n2, TcTile* t13, TcTile* t2) {
+  pdl_launch_dependents();  // let the next kernel on the stream launch early
+  pdl_wait();               // inputs written by the previous kernel are visible
+  __shared__ int s_ids[16][32];
+  __shared__ float s_sel[16][32];
+  __shared__ float s_w[16][32];
+  __shared__ float s_row[16][258];
+  const int warp = threadIdx.x >> 5;
+  if (warp < 16)
+    for (int t = warp; t < T; t += 16)
+      topk_token_stage<8>(logits, part, nsplit, t, T, E, E1, k, norm_topk, ids, w, nullptr, s_ids[warp],
+                          s_sel[warp], s_w[warp], s_row[warp]);
+  __syncthreads();  // the ids written above are visible to the whole CTA
+  group_stage(ids, T, k, E, has_shared, counts, offsets, perm, nullptr, 0, ctrl);
   __syncthreads();
-  if (warp == 0) {
-    unsigned long long s = wtot[lane];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const unsigned long long yv = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += yv;
-    }
-    wtot[lane] = s;
-  }
-  __syncthreads();
-  const unsigned long long before = incl - v + (warp ? wtot[warp - 1] : 0ull);
-  const int b13 = static_cast<int>(before >> 32), b2 = static_cast<int>(before & 0xffffffffu);
-  if (2 * tid < n) { pre13[2 * tid] = b13; pre2[2 * tid] = b2; }
-  if (2 * tid + 1 < n) { pre13[2 * tid + 1] = b13 + a13[0]; pre2[2 * tid + 1] = b2 + a2[0]; }
-  __syncthreads();
-  const int tot13 = static_cast<int>(wtot[31] >> 32), tot2 = static_cast<int>(wtot[31] & 0xffffffffu);
-  if (tid == 0) { *n13 = tot13; *n2 = tot2; }
-  // Fill both lists in parallel: tile i belongs to the last expert whose first
-  // tile index is <= i (experts without tiles share their successor's start).
-  for (int i = tid; i < tot13 + tot2; i += 1024) {
-    const bool second = i >= tot13;
-    const int ii = second ? i - tot13 : i;
-    const int* pre = second ? pre2 : pre13;
-    int lo = 0, hi = n - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (pre[mid] <= ii) lo = mid; else hi = mid - 1;
-    }
-    const int e = lo;
-    const int ie = e == E ? Is : I;
-    const int per_n = second ? (H / 128 + mt2 - 1) / mt2 : (ie / 64 + mt13 - 1) / mt13;  // M-groups per N-tile
-    const int j = (ii - pre[e]) / per_n, mm = (ii - pre[e]) - j * per_n;
-    const int cnt = counts[e];
-    const TcTile tl{e, mm, offsets[e] + j * N, min(N, cnt - j * N)};
-    if (second) t2[ii] = tl; else t13[ii] = tl;
-  }
+  schedule_stage(counts, offsets, E, I, Is, H, N, mt13, mt2, n13, n2, t13, t2);
 }
 
 // Xs[pos, :] = x[token of perm[pos], :]: one warp per row, 16-byte chunks,
@@ -805,7 +768,7 @@ constexpr int kMT = 2;
 
 template <int N>
 static moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws, const WsLayout& L,
-                                     int32_t T, cudaStream_t st) {
+                                     int32_t T, int fused_nsplit, cudaStream_t st) {
   constexpr int DT = MOE_BF16;
   const int H = c.hidden, E = c.n_experts, k = c.top_k, I = c.inter, Is = c.shared_inter;
   const int Imax = I > Is ? I : Is;
@@ -830,9 +793,19 @@ static moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uin
   // M-tile per CTA then spreads the weight stream over twice the SMs.
   const int sms0 = sm_count();
   const int est13 = (T * k < E ? T * k : E) * ((I / 64 + kMT - 1) / kMT);  // W13 tiles with kMT
-  const int mt13 = 2 * est13 <= sms0 ? 1 : kMT;
-  launch_pdl(tc_schedule_kernel, dim3(1), dim3(1024), 0, st, counts, offsets, E, I, Is, H, N, mt13, kMT, sched, sched + 1, t13, t2);
-  if (moe_status_t s = check_launch("tc_schedule_kernel")) return s;
+  const int mt13 = est13 <= sms0 ? 1 : kMT;
+  if (fused_nsplit >= 0) {  // ranking + grouping + tile lists in one launch (small batches)
+    float* lg = reinterpret_cast<float*>(ws + L.r_logits);
+    const int E1 = c.has_shared_gate ? E + 1 : E;
+    launch_pdl(route_group_kernel, dim3(1), dim3(1024), 0, st, lg, reinterpret_cast<const float*>(ws + L.r_part),
+               fused_nsplit, T, E, E1, k, c.norm_topk, p.topk_ids, p.topk_w, Is > 0 ? 1 : 0, counts, offsets, perm,
+               ctrl, I, Is, H, N, mt13, kMT, sched, sched + 1, t13, t2);
+    if (moe_status_t s = check_launch("route_group_kernel")) return s;
+  } else {
+    launch_pdl(tc_schedule_kernel, dim3(1), dim3(1024), 0, st, counts, offsets, E, I, Is, H, N, mt13, kMT, sched,
+               sched + 1, t13, t2);
+    if (moe_status_t s = check_launch("tc_schedule_kernel")) return s;
+  }
   const int sms = sm_count();
   const int gg = (P + 7) / 8 < sms * 8 ? (P + 7) / 8 : sms * 8;
   launch_pdl(tc_gather_kernel, dim3(gg), dim3(256), 0, st, static_cast<const uint8_t*>(p.x), perm, P, T, k, H, xs);
@@ -915,9 +888,9 @@ int tc_tile_n(const moe_cfg_t& c, int32_t T) {
 }
 
 moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws, const WsLayout& L, int32_t T,
-                              cudaStream_t st) {
-  if (L.tc_n == 128) return launch_tc_passes<128>(c, p, ws, L, T, st);
-  return launch_tc_passes<64>(c, p, ws, L, T, st);
+                              int fused_nsplit, cudaStream_t st) {
+  if (L.tc_n == 128) return launch_tc_passes<128>(c, p, ws, L, T, fused_nsplit, st);
+  return launch_tc_passes<64>(c, p, ws, L, T, fused_nsplit, st);
 }
 
 }  // namespace moe

@@ -83,9 +83,12 @@ struct BlockPtrs {
 // Kernel launchers (each returns MOE_OK or a host-side error).
 moe_status_t launch_decode_fused(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws,
                                  const WsLayout& L, cudaStream_t st);
+// With nsplit_out != NULL the top-k launch is skipped and *nsplit_out tells
+// how the logits were left (split partial sums, or 0: plain [T, E1] rows).
 moe_status_t launch_router(const moe_cfg_t& c, const void* x, const void* router_w,
                            const void* shared_gate_w, int32_t T, int32_t* ids, float* w,
-                           float* logits_out, uint8_t* ws, const WsLayout& L, cudaStream_t st);
+                           float* logits_out, uint8_t* ws, const WsLayout& L, cudaStream_t st,
+                           int* nsplit_out = nullptr);
 moe_status_t launch_grouped(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws, const WsLayout& L,
                             int32_t T, cudaStream_t st);
 moe_status_t launch_wait_test(uint8_t* ws, cudaStream_t st);
@@ -98,8 +101,11 @@ struct Control;
 bool tc_router_supported(const moe_cfg_t& c);
 moe_status_t launch_tc_router(const moe_cfg_t& c, const void* x, const void* router_w, const void* gate_w,
                               int32_t T, float* logits, int E1, Control* ctrl, cudaStream_t st);
+// fused_nsplit >= 0: the router ran without its top-k (logits as that many
+// split partial sums, 0 = plain); ranking, grouping and the tile lists then run
+// as one launch.  -1: ids and the grouping are already in the workspace.
 moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws, const WsLayout& L, int32_t T,
-                              cudaStream_t st);
+                              int fused_nsplit, cudaStream_t st);
 
 // Launch with programmatic stream serialization: the kernel may be scheduled
 // while the previous kernel on the stream drains.  Every kernel of the library

@@ -12,6 +12,7 @@
 
 #include "moe_common.cuh"
 #include "moe_internal.h"
+#include "moe_stages.cuh"
 
 namespace moe {
 
@@ -241,6 +242,7 @@ __global__ void __launch_bounds__(256) router_mma_kernel(const uint8_t* __restri
 // With nsplit > 0 the logits arrive as nsplit partial sums part[s][t][e]
 // (router_mma_kernel): they are added in split order, stored into `logits`
 // (the [T, E1] buffer later kernels read) and ranked from shared memory.
+// One warp per token: rank, weights, outputs.
 template <int MAXM>
 __global__ void __launch_bounds__(256) router_topk_kernel(float* __restrict__ logits, const float* __restrict__ part,
                                                           int nsplit, int T, int E, int E1, int k, int norm_topk,
@@ -250,39 +252,18 @@ __global__ void __launch_bounds__(256) router_topk_kernel(float* __restrict__ lo
   __shared__ int s_ids[8][32];
   __shared__ float s_sel[8][32];
   __shared__ float s_w[8][32];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ float s_row[8][MAXM == 8 ? 258 : 1];
+  const int warp = threadIdx.x >> 5;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
-  __shared__ float s_row[8][MAXM == 8 ? 258 : 1];
-  const float* row = logits + static_cast<size_t>(t) * E1;
-  if constexpr (MAXM == 8) {
-    if (nsplit > 0) {
-      for (int e = lane; e < E1; e += 32) {
-        float v = 0.0f;
-        for (int sp = 0; sp < nsplit; ++sp) v += part[(static_cast<size_t>(sp) * T + t) * E1 + e];
-        s_row[warp][e] = v;
-        logits[static_cast<size_t>(t) * E1 + e] = v;
-      }
-      __syncwarp();
-      row = s_row[warp];
-    }
-  }
-  if constexpr (MAXM == 8) warp_topk_sorted8(row, E, k, s_ids[warp], s_sel[warp]);
-  else warp_topk<MAXM>(row, E, k, s_ids[warp], s_sel[warp]);
-  __syncwarp();
-  warp_routing_weights(row, E, s_sel[warp], k, norm_topk, s_w[warp]);
-  __syncwarp();
-  if (lane < k) {
-    ids[static_cast<size_t>(t) * k + lane] = s_ids[warp][lane];
-    w[static_cast<size_t>(t) * k + lane] = s_w[warp][lane];
-  }
-  if (logits_out)
-    for (int e = lane; e < E; e += 32) logits_out[static_cast<size_t>(t) * E + e] = row[e];
+  topk_token_stage<MAXM>(logits, part, nsplit, t, T, E, E1, k, norm_topk, ids, w, logits_out, s_ids[warp],
+                         s_sel[warp], s_w[warp], s_row[warp]);
 }
 
 moe_status_t launch_router(const moe_cfg_t& c, const void* x, const void* router_w,
                            const void* shared_gate_w, int32_t T, int32_t* ids, float* w,
-                           float* logits_out, uint8_t* ws, const WsLayout& L, cudaStream_t st) {
+                           float* logits_out, uint8_t* ws, const WsLayout& L, cudaStream_t st,
+                           int* nsplit_out) {
   const int E = c.n_experts;
   const int E1 = E + 1;
   float* lg = reinterpret_cast<float*>(ws + L.r_logits);
@@ -328,6 +309,11 @@ moe_status_t launch_router(const moe_cfg_t& c, const void* x, const void* router
       launch_pdl(router_logits_kernel<MOE_F16>, dim3(g1), dim3(256), 0, st, xb, wb, swg, T, c.hidden, E, stride, lg);
   }
   if (moe_status_t s = check_launch("router_logits_kernel")) return s;
+  if (nsplit_out) {  // the caller ranks (fused with its grouping)
+    *nsplit_out = nsplit;
+    stat_kernels(1);
+    return MOE_OK;
+  }
   // The logits rows are laid out with stride E1 only when the gate column exists.
   dim3 g2((T + 7) / 8);
   if (E <= 256)
