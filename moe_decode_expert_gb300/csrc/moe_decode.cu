@@ -601,12 +601,13 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
   // rows), B columns 0-2 = the activation terms, fp32 accumulation.  Lane t of
   // a B fragment needs columns 2t, 2t+1, 2t+8, 2t+9 of a step, kept at
   // 4t..4t+3 of the step's 16 slots.
-  cp_async_wait_all();  // this thread's W2 copies
   // One thread per CTA counts CTAs in and waits for all G of them before any
   // warp reads the activation words: every warp polling the words while other
   // CTAs are still producing floods L2 with re-reads and slows the weight
   // streams.  After the count the words have (nearly always) landed and each
   // warp's gather is one round trip (the epoch tags still catch a late one).
+  // A CTA counts itself in as soon as its activations are out; its own W2
+  // copies land while it waits.
   __syncthreads();
   if (tid == 0 && !s_fail) {
     uint32_t* cnt = &a.ctrl->arrive[epoch & 1u];
@@ -618,6 +619,7 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
     }
     if (!arrived) s_fail = kDevTimeoutAct;
   }
+  cp_async_wait_all();  // this thread's W2 copies
   __syncthreads();
   {
     const int g = lane >> 2, t = lane & 3;
