@@ -259,3 +259,59 @@ def test_timeout_path_records_and_recovers(m):
     ref = oracle_full(wl, d)
     assert np.array_equal(ids.cpu().numpy(), ref["ids"])
     parity(out, ref["out"])
+
+
+@pytest.mark.parametrize("flags", [0, 4], ids=["plain", "static_weights"])
+def test_chained_layers_read_the_previous_output(m, flags):
+    """Each layer's x is the previous layer's out, written by the previous kernel
+    on the stream.  A layer kernel launches early (programmatic dependent launch;
+    with static weights it also streams weights and prefetches x into L2 before
+    its wait) but must read x only after the previous layer has completed.
+    Eager and graph-replayed chains agree bit for bit, and every layer matches the
+    oracle run on the input the GPU actually used."""
+    wl = moe_synth.workload("sharded_decode")  # fp16 in and out, so out can feed the next layer
+    cfg = m.cfg_from_workload(wl, None, flags)
+    L = 4
+    layers = []
+    for l in range(L):
+        g = moe_synth.make_layer(wl, l, 1, device=DEV, weights_only=True)
+        # larger down projections keep the chained activations near unit scale
+        g["w2"] = (g["w2"].float() * 8).to(g["w2"].dtype)
+        g["shared_w2"] = (g["shared_w2"].float() * 8).to(g["shared_w2"].dtype)
+        layers.append(g)
+    bufs = [moe_synth.make_x(wl, 0, 1, DEV)] + [torch.empty(1, wl.hidden, dtype=wl.torch_dtype, device=DEV)
+                                                for _ in range(L)]
+    ids = [torch.empty(1, wl.top_k, dtype=torch.int32, device=DEV) for _ in range(L)]
+    wts = [torch.empty(1, wl.top_k, dtype=torch.float32, device=DEV) for _ in range(L)]
+    ws = m.alloc_workspace(cfg, 1, DEV)
+
+    def step():
+        for l, g in enumerate(layers):
+            m.moe_decode_forward(cfg, bufs[l], g["router_w"], g["w13"], g["w2"], g["shared_w13"], g["shared_w2"],
+                                 g["shared_gate_w"], ids[l], wts[l], bufs[l + 1], ws)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.synchronize()
+    m.moe_query_status(ws)
+    for l, g in enumerate(layers):
+        ref = oracle_sampled(wl, {**g, "x": bufs[l]}, [0])
+        lg = ref["logits"]
+        if min_rank_gap(lg, wl.top_k)[0] > 1e-4 * np.abs(lg).max():
+            assert np.array_equal(ids[l].cpu().numpy(), ref["ids"])
+        parity(bufs[l + 1], ref["out"])
+        assert 0.05 < bufs[l + 1].float().abs().max().item() < 1e3
+    eager = [b.clone() for b in bufs[1:]]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        step()
+    for b in bufs[1:]:
+        b.zero_()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    m.moe_query_status(ws)
+    for a, b in zip(eager, bufs[1:]):
+        assert torch.equal(a, b)
