@@ -159,11 +159,11 @@ def barrier(ws: int):
 
 
 # ------------------------------------------------------------------ oracle
-def oracle_sample(wl, layers, max_seconds, get_layer):
+def oracle_sample(wl, layers, max_seconds, get_layer, warmup=0):
     """Time the CPU oracle on (layer, token) samples of the workload: returns
     (seconds, layers evaluated).  Inputs are copied to the host outside the
     timed part; the oracle routes on the host and reads only the experts it
-    selects."""
+    selects.  The first ``warmup`` evaluations (of layer 0) are not timed."""
     import oracle
     c = oracle.OracleCfg(wl.hidden, wl.n_experts, wl.top_k, wl.inter, wl.shared_inter, wl.dtype,
                          wl.norm_topk, wl.has_shared_gate)
@@ -177,6 +177,8 @@ def oracle_sample(wl, layers, max_seconds, get_layer):
         w2 = {int(e): b(g["w2"][int(e)]) for e in ids}
         sh = (b(g["shared_w13"]), b(g["shared_w2"]), b(g["shared_gate_w"]))
         del g
+        for _ in range(warmup if l == 0 else 0):
+            oracle.moe_forward(c, x, wr, w13, w2, *sh)
         t0 = time.perf_counter()
         oracle.moe_forward(c, x, wr, w13, w2, *sh)
         spent += time.perf_counter() - t0
@@ -191,17 +193,19 @@ def run_reference(args, wl, ws_, rank):
         return
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     budget = min(30.0, max(5.0, 0.002 * (args.steps + args.warmup)))
-    spent, n = oracle_sample(wl, wl.layers, budget, lambda l: moe_synth.make_layer(wl, l, 1, device=dev))
+    spent, n = oracle_sample(wl, wl.layers, budget, lambda l: moe_synth.make_layer(wl, l, 1, device=dev),
+                             warmup=args.warmup)
     s_per_layer = spent / n
     value = 1.0 / (s_per_layer * wl.layers)   # tokens/s through the 36-layer stack
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "impl": "reference", "n_gpus": args.gpus,
-        "steps": n, "warmup": 0, "ms_per_step": s_per_layer * wl.layers * 1e3, "higher_is_better": True,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": s_per_layer * wl.layers * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_of(wl),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{n} layers x 1 token of the workload, {spent:.1f} s of oracle time, "
-                                   f"scaled to the {wl.layers}-layer step"},
+                         "sample": f"{n} layers x 1 token of the workload after {args.warmup} untimed "
+                                   f"warm-up calls, {spent:.1f} s of oracle time, scaled to the "
+                                   f"{wl.layers}-layer step"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
