@@ -46,13 +46,33 @@ def algorithmic_bytes(wl, T=1) -> int:
     return 2 * n + 2 * T * H * 2
 
 
-def kernel_source_hash() -> str:
-    """Hash of the sources the single-launch decode kernel is built from."""
+def code_lines(text):
+    """The lines of a C++/CUDA source with // comments, trailing blanks and
+    empty lines removed (a '//' after an odd number of quotes is inside a
+    string and kept), so that comment-only edits keep the hash."""
+    out = []
+    for line in text.splitlines():
+        i = line.find("//")
+        while i >= 0 and line.count('"', 0, i) % 2 == 1:
+            i = line.find("//", i + 2)
+        code = (line[:i] if i >= 0 else line).rstrip()
+        if code:
+            out.append(code)
+    return out
+
+
+def kernel_source_hash(read=None) -> str:
+    """Hash of the code (comments excluded) the single-launch decode kernel is
+    built from."""
     import hashlib
     h = hashlib.sha256()
     for f in ("moe_decode.cu", "moe_common.cuh"):
-        with open(os.path.join(ROOT, "moe_decode_expert_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        if read is None:
+            with open(os.path.join(ROOT, "moe_decode_expert_gb300", "csrc", f)) as fh:
+                text = fh.read()
+        else:
+            text = read(f)
+        h.update("\n".join(code_lines(text)).encode())
     return h.hexdigest()[:16]
 
 

@@ -10,24 +10,30 @@
 // How (GB300 design, not the pages' BI-V100 kernels): one CTA per SM, each
 // owning a slice of every phase, all phases in one launch.
 //   phase 1  routing-independent rows — router rows, the shared gate row and
-//            the shared expert's gate/up pairs — as warp-per-row dot products
-//            with 16-byte streaming loads issued before x lands in smem;
-//            results are published as (value, epoch) exchange words.
-//   phase 2  every CTA gathers the E logits (one L2 round trip when they are
-//            all published), and one warp ranks them (fp32, lower index wins
-//            ties) and forms the routing weights; no grid barrier and no
-//            second kernel.
-//   phase 3  thread 0 bulk-copies (TMA, untiled) the selected experts' W2
-//            rows of this CTA's output slice into smem while the warps
-//            compute this CTA's share of the k*I routed gate/up pairs
-//            (W13 rows streamed to registers), apply SiLU*up and publish act.
-//   phase 4  every CTA gathers all k*I + Is activations, waits for its W2
-//            rows, and computes its slice of out[h] = sum_j w_j (W2_j act_j)
-//            + g (Ws2 sact).
-// The two exchanges replace two kernel boundaries; each wait is bounded by
-// the GPU global timer and records an error instead of hanging.  The kernel
-// triggers programmatic dependent launch at entry so the next call on the
-// stream launches early and waits in its own prologue.
+//            the shared expert's gate/up pairs — as one CTA GEMV on m16n8k16
+//            tensor-core steps (weight rows = A, x = column 0 of B), columns
+//            split over the warps; the first loads go out before the PDL wait
+//            when the weights are static.  Results are published as
+//            (value, epoch) exchange words.
+//   phase 2  every CTA gathers the E logits (one L2 round trip once they are
+//            all published) and ranks them itself (fp32, lower index wins
+//            ties): per-warp top-k, then an exact ranking of the candidates;
+//            warp 0 forms the routing weights.  No grid barrier, no second
+//            kernel.
+//   phase 3  this CTA's share of the k*I routed gate/up pairs (a CTA GEMV as
+//            in phase 1, or two pairs in flight per warp on wide shapes),
+//            SiLU*up times the routing weight published per pair; meanwhile
+//            each warp copies (cp.async) the W2 columns it needs in phase 4
+//            into padded shared-memory rows.
+//   phase 4  after an arrival counter shows every CTA's activations out, each
+//            warp gathers the activations of its column range, splits them
+//            into three storage-type terms and runs m16n8k16 steps over its
+//            W2 columns: out[h] = sum_j w_j (W2_j act_j) + g (Ws2 sact) for
+//            this CTA's output rows, the warps' partial rows summed in order.
+// Each exchange wait is bounded by the GPU global timer and records an
+// error instead of hanging.  The kernel triggers programmatic dependent launch
+// at entry so the next call on the stream launches early and waits in its own
+// prologue.
 
 #include "moe_common.cuh"
 #include "moe_internal.h"
