@@ -59,13 +59,19 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // --------------------------------------------------------------- loads
+// Loads in kernels launched with programmatic dependent launch are volatile
+// asm (or plain loads through pointers without __restrict__): the compiler
+// then keeps them after griddepcontrol.wait.  A non-volatile asm load, or a
+// load through a const __restrict__ kernel parameter (an invariant load to
+// the compiler), may be scheduled above the wait and read stale data.
+//
 // 16-byte streaming load of read-only weights: not kept in L1, with a 256-byte
 // L2 prefetch hint (consecutive lanes read consecutive 16-byte chunks).
 __device__ __forceinline__ uint4 ld_stream16(const void* p) {
   uint4 r;
-  asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
-      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-      : "l"(p));
+  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
   return r;
 }
 
@@ -97,9 +103,9 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 
 __device__ __forceinline__ uint4 ld_nc16(const void* p) {
   uint4 r;
-  asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
-      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-      : "l"(p));
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
   return r;
 }
 

@@ -31,7 +31,7 @@ constexpr int kHB = 64;           // output rows per w2 work item
 
 // ------------------------------------------------------------- grouping
 // One CTA of 1024 threads.  counts/offsets/tiles live in the workspace.
-__global__ void __launch_bounds__(1024) group_kernel(const int32_t* __restrict__ ids, int T, int k, int E,
+__global__ void __launch_bounds__(1024) group_kernel(const int32_t* ids, int T, int k, int E,
                                                      int has_shared, int32_t* counts_out,
                                                      int32_t* offsets, int32_t* perm, int32_t* tiles,
                                                      int write_tiles, Control* ctrl) {
@@ -46,9 +46,9 @@ __device__ __forceinline__ int pair_token(int p, int T, int k) { return p < T * 
 // ----------------------------------------------------------- W13 + SiLU
 template <int DT>
 __global__ void __launch_bounds__(kGThreads) grouped_w13_kernel(
-    const uint8_t* __restrict__ x, const uint8_t* __restrict__ w13, const uint8_t* __restrict__ sw13,
-    const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets,
-    const int32_t* __restrict__ perm, const int32_t* __restrict__ tiles, int T, int H, int E, int k,
+    const uint8_t* x, const uint8_t* w13, const uint8_t* sw13,
+    const int32_t* counts, const int32_t* offsets,
+    const int32_t* perm, const int32_t* tiles, int T, int H, int E, int k,
     int I, int Is, int act_stride, float* __restrict__ act) {
   pdl_launch_dependents();  // let the next kernel on the stream launch early
   pdl_wait();               // inputs written by the previous kernel are visible
@@ -115,11 +115,11 @@ __global__ void __launch_bounds__(kGThreads) grouped_w13_kernel(
 // ------------------------------------------------------ W2 + pair weight
 template <int DT>
 __global__ void __launch_bounds__(kGThreads) grouped_w2_kernel(
-    const uint8_t* __restrict__ w2, const uint8_t* __restrict__ sw2, const int32_t* __restrict__ counts,
-    const int32_t* __restrict__ offsets, const int32_t* __restrict__ perm,
-    const int32_t* __restrict__ tiles, const float* __restrict__ topk_w,
-    const float* __restrict__ gate_logits, int gate_stride, int has_gate, int T, int H, int E, int k,
-    int I, int Is, int act_stride, const float* __restrict__ act, float* __restrict__ y) {
+    const uint8_t* w2, const uint8_t* sw2, const int32_t* counts,
+    const int32_t* offsets, const int32_t* perm,
+    const int32_t* tiles, const float* topk_w,
+    const float* gate_logits, int gate_stride, int has_gate, int T, int H, int E, int k,
+    int I, int Is, int act_stride, const float* act, float* __restrict__ y) {
   pdl_launch_dependents();  // let the next kernel on the stream launch early
   pdl_wait();               // inputs written by the previous kernel are visible
   extern __shared__ __align__(16) float as[];   // [kTN][Imax] fp32
@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(kGThreads) grouped_w2_kernel(
 }
 
 // ---------------------------------------------------------------- combine
-__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, int T, int H, int k,
+__global__ void __launch_bounds__(256) combine_kernel(const float* y, int T, int H, int k,
                                                       int has_shared, void* out, int out_dtype) {
   pdl_launch_dependents();  // let the next kernel on the stream launch early
   pdl_wait();               // inputs written by the previous kernel are visible

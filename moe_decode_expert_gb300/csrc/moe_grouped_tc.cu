@@ -48,6 +48,12 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
       : "memory");
 }
+// Fetch a tensor map (a __grid_constant__ kernel parameter) ahead of its first
+// TMA copy.
+__device__ __forceinline__ void tensormap_prefetch(const CUtensorMap* m) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
                : "memory");
@@ -152,11 +158,10 @@ __device__ __forceinline__ bool epi_any(bool v) {
 template <int DT, int N, int MT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_w13_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapAs,
-                  const __grid_constant__ CUtensorMap mapB, const TcTile* __restrict__ tiles,
-                  const int32_t* __restrict__ n_tiles_p, int H, int I, int Is, int E, int act_stride,
+                  const __grid_constant__ CUtensorMap mapB, const TcTile* tiles,
+                  const int32_t* n_tiles_p, int H, int I, int Is, int E, int act_stride,
                   uint16_t* __restrict__ act_hi, uint16_t* __restrict__ act_lo, Control* ctrl, uint64_t timeout) {
   pdl_launch_dependents();  // let the next kernel on the stream launch early
-  pdl_wait();               // inputs written by the previous kernel are visible
   constexpr uint32_t kStage = MT * kTileA + N * 128;
   constexpr int kStg = 128 * 17 * 4;
   constexpr int kStages = (kSmemBudget - kStg) / kStage > 8 ? 8 : (kSmemBudget - kStg) / kStage;
@@ -175,6 +180,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(&done, 1);
     mbar_fence_init();
     s_abort = 0;
+    tensormap_prefetch(&mapA);
+    tensormap_prefetch(&mapAs);
+    tensormap_prefetch(&mapB);
   }
   if (warp == 1) {
     tmem_alloc(&tmem_base_s, kCols);
@@ -183,6 +191,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // The set-up above reads nothing an earlier kernel writes; from here on the
+  // tile list and the operands it wrote are read.
+  pdl_wait();
   const uint32_t tbase = tmem_base_s;
   const int ntiles = *n_tiles_p;
   const int KB = H / kBK;
@@ -329,12 +340,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_w2_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapAs,
                  const __grid_constant__ CUtensorMap mapHi, const __grid_constant__ CUtensorMap mapLo,
                  const __grid_constant__ CUtensorMap mapHiS, const __grid_constant__ CUtensorMap mapLoS,
-                 const TcTile* __restrict__ tiles, const int32_t* __restrict__ n_tiles_p,
-                 const int32_t* __restrict__ perm, const float* __restrict__ topk_w,
-                 const float* __restrict__ gate_logits, int gate_stride, int has_gate, int T, int H, int I, int Is,
+                 const TcTile* tiles, const int32_t* n_tiles_p,
+                 const int32_t* perm, const float* topk_w,
+                 const float* gate_logits, int gate_stride, int has_gate, int T, int H, int I, int Is,
                  int E, int k, float* __restrict__ y, Control* ctrl, uint64_t timeout) {
   pdl_launch_dependents();  // let the next kernel on the stream launch early
-  pdl_wait();               // inputs written by the previous kernel are visible
   constexpr uint32_t kStage = MT * kTileA + 2 * N * 128;
   constexpr int kStages = kSmemBudget / kStage > 8 ? 8 : kSmemBudget / kStage;
   constexpr uint32_t kCols = 2 * MT * N;
@@ -353,6 +363,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(&done, 1);
     mbar_fence_init();
     s_abort = 0;
+    tensormap_prefetch(&mapA);
+    tensormap_prefetch(&mapAs);
+    tensormap_prefetch(&mapHi);
+    tensormap_prefetch(&mapLo);
+    tensormap_prefetch(&mapHiS);
+    tensormap_prefetch(&mapLoS);
   }
   if (warp == 1) {
     tmem_alloc(&tmem_base_s, kCols);
@@ -361,6 +377,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // The set-up above reads nothing an earlier kernel writes; from here on the
+  // tile list and the operands it wrote are read.
+  pdl_wait();
   const uint32_t tbase = tmem_base_s;
   const int ntiles = *n_tiles_p;
   const int mtiles = H / 128;
@@ -510,7 +529,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                      const __grid_constant__ CUtensorMap mapX, int T, int H, int E, int E1, int mE, int nm,
                      float* __restrict__ logits, Control* ctrl, uint64_t timeout) {
   pdl_launch_dependents();  // let the next kernel on the stream launch early
-  pdl_wait();               // inputs written by the previous kernel are visible
   constexpr uint32_t kStage = kTileA + N * 128;
   constexpr int kStages = kSmemBudget / kStage > 8 ? 8 : kSmemBudget / kStage;
   extern __shared__ uint8_t smem_raw[];
@@ -526,6 +544,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(&done, 1);
     mbar_fence_init();
     s_abort = 0;
+    tensormap_prefetch(&mapWr);
+    tensormap_prefetch(&mapG);
+    tensormap_prefetch(&mapX);
   }
   if (warp == 1) {
     tmem_alloc(&tmem_base_s, 2 * N);
@@ -534,6 +555,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // The set-up above reads nothing an earlier kernel writes; from here on the
+  // tile list and the operands it wrote are read.
+  pdl_wait();
   const uint32_t tbase = tmem_base_s;
   const int ntiles = nm * ((T + N - 1) / N);
   const int KB = H / kBK;
@@ -649,8 +673,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // ===================================================== schedule + gather
 // Tile lists of both passes from the per-expert counts/offsets (one CTA).
 // Layout of `sched`: [0] n13, [1] n2, then TcTile arrays at the offsets given.
-__global__ void __launch_bounds__(1024) tc_schedule_kernel(const int32_t* __restrict__ counts,
-                                                           const int32_t* __restrict__ offsets, int E, int I,
+__global__ void __launch_bounds__(1024) tc_schedule_kernel(const int32_t* counts,
+                                                           const int32_t* offsets, int E, int I,
                                                            int Is, int H, int N, int mt13, int mt2, int32_t* n13,
                                                            int32_t* n2, TcTile* t13, TcTile* t2) {
   pdl_launch_dependents();  // let the next kernel on the stream launch early
@@ -661,9 +685,11 @@ __global__ void __launch_bounds__(1024) tc_schedule_kernel(const int32_t* __rest
 // Very small batches (T <= 8, E <= 256): the ranking of every token, the counting
 // sort of the pairs by expert and the tile lists of both tensor-core passes in
 // one single-CTA launch instead of three (each of those kernels is a few µs of
-// mostly fixed latency at this size).  Warps 0-15 rank the tokens, then all
-// 1024 threads group and schedule.
-__global__ void __launch_bounds__(1024) route_group_kernel(float* __restrict__ logits, const float* __restrict__ part,
+// mostly fixed latency at this size).  All 1024 threads add the router's split
+// partial sums (every load in flight at once), warp t ranks token t, then all
+// threads group and schedule; ids, counts and offsets pass between the stages
+// in shared memory.
+__global__ void __launch_bounds__(1024) route_group_kernel(float* logits, const float* part,
                                                            int nsplit, int T, int E, int E1, int k, int norm_topk,
                                                            int32_t* ids, float* w, int has_shared, int32_t* counts,
                                                            int32_t* offsets, int32_t* perm, Control* ctrl, int I,
@@ -671,24 +697,51 @@ __global__ void __launch_bounds__(1024) route_group_kernel(float* __restrict__ l
                                                            int32_t* n2, TcTile* t13, TcTile* t2) {
   pdl_launch_dependents();  // let the next kernel on the stream launch early
   pdl_wait();               // inputs written by the previous kernel are visible
-  __shared__ int s_ids[16][32];
-  __shared__ float s_sel[16][32];
-  __shared__ float s_w[16][32];
-  __shared__ float s_row[16][258];
-  const int warp = threadIdx.x >> 5;
-  if (warp < 16)
-    for (int t = warp; t < T; t += 16)
-      topk_token_stage<8>(logits, part, nsplit, t, T, E, E1, k, norm_topk, ids, w, nullptr, s_ids[warp],
-                          s_sel[warp], s_w[warp], s_row[warp]);
-  __syncthreads();  // the ids written above are visible to the whole CTA
-  group_stage(ids, T, k, E, has_shared, counts, offsets, perm, nullptr, 0, ctrl);
+  // T <= 8 and E1 <= 257 (checked on the host)
+  __shared__ float s_lg[8 * 258];  // the T rows of logits
+  __shared__ int s_ids[8][32];
+  __shared__ float s_sel[8][32];
+  __shared__ float s_w[8][32];
+  __shared__ int32_t s_flat[8 * 32];  // ids [T, k]
+  __shared__ int32_t s_cnt[258], s_off[258];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // The logits: the router's split partial sums added by every thread (all
+  // loads in flight at once), or the finished rows copied.
+  for (int q0 = tid; q0 < T * E1; q0 += 1024 * kSumCols) {
+    float v[kSumCols];
+    if (nsplit > 0) {
+      sum_splits(part, nsplit, static_cast<size_t>(T) * E1, q0, 1024, T * E1, v);
+    } else {
+#pragma unroll
+      for (int c = 0; c < kSumCols; ++c) {
+        const int q = q0 + 1024 * c;
+        v[c] = q < T * E1 ? logits[q] : 0.0f;
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < kSumCols; ++c) {
+      const int q = q0 + 1024 * c;
+      if (q < T * E1) {
+        s_lg[q] = v[c];
+        if (nsplit > 0) logits[q] = v[c];  // [T, E1] rows read by later kernels
+      }
+    }
+  }
   __syncthreads();
-  schedule_stage(counts, offsets, E, I, Is, H, N, mt13, mt2, n13, n2, t13, t2);
+  if (warp < T) {
+    topk_token_stage<8>(s_lg, nullptr, 0, warp, T, E, E1, k, norm_topk, ids, w, nullptr, s_ids[warp], s_sel[warp],
+                        s_w[warp], nullptr);
+    if (lane < k) s_flat[warp * k + lane] = s_ids[warp][lane];
+  }
+  __syncthreads();
+  group_stage(s_flat, T, k, E, has_shared, counts, offsets, perm, nullptr, 0, ctrl, s_cnt, s_off);
+  __syncthreads();
+  schedule_stage(s_cnt, s_off, E, I, Is, H, N, mt13, mt2, n13, n2, t13, t2);
 }
 
 // Xs[pos, :] = x[token of perm[pos], :]: one warp per row, 16-byte chunks,
 // up to 8 chunks per lane in flight.
-__global__ void __launch_bounds__(256) tc_gather_kernel(const uint8_t* __restrict__ x, const int32_t* __restrict__ perm,
+__global__ void __launch_bounds__(256) tc_gather_kernel(const uint8_t* x, const int32_t* perm,
                                                         int P, int T, int k, int H, uint8_t* __restrict__ xs) {
   pdl_launch_dependents();  // let the next kernel on the stream launch early
   pdl_wait();               // inputs written by the previous kernel are visible

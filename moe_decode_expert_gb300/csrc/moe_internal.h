@@ -109,8 +109,11 @@ moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* w
 
 // Launch with programmatic stream serialization: the kernel may be scheduled
 // while the previous kernel on the stream drains.  Every kernel of the library
-// runs griddepcontrol.wait before touching memory, so ordering is unchanged;
-// only the launch latency overlaps.
+// runs griddepcontrol.wait before it reads anything an earlier kernel may
+// write (only set-up that reads no such memory — barrier initialisation, TMEM
+// allocation, tensor-map prefetch, weight loads with static weights — may come
+// first), and those reads are loads the compiler cannot move above the wait,
+// so ordering is unchanged; only the launch latency overlaps.
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
                               Args&&... args) {

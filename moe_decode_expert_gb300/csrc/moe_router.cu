@@ -23,9 +23,9 @@ constexpr int kRouterGemvMaxT = 64;  // T up to this uses the row-per-warp kerne
 constexpr int kRouterTcMinT = 256;   // bf16 and T from this on: tensor-core router
 
 template <int DT>
-__global__ void __launch_bounds__(256) router_logits_kernel(const uint8_t* __restrict__ x,
-                                                            const uint8_t* __restrict__ wr,
-                                                            const uint8_t* __restrict__ swg, int T,
+__global__ void __launch_bounds__(256) router_logits_kernel(const uint8_t* x,
+                                                            const uint8_t* wr,
+                                                            const uint8_t* swg, int T,
                                                             int H, int E, int E1, float* __restrict__ logits) {
   pdl_launch_dependents();  // let the next kernel on the stream launch early
   pdl_wait();               // inputs written by the previous kernel are visible
@@ -84,9 +84,9 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const uint8_t* __res
 // fp32.  Grid (ceil(E1 / 8), ceil(T / 16)).
 constexpr int kGvTok = 16;
 template <int DT>
-__global__ void __launch_bounds__(256) router_gemv_kernel(const uint8_t* __restrict__ x,
-                                                          const uint8_t* __restrict__ wr,
-                                                          const uint8_t* __restrict__ swg, int T, int H, int E,
+__global__ void __launch_bounds__(256) router_gemv_kernel(const uint8_t* x,
+                                                          const uint8_t* wr,
+                                                          const uint8_t* swg, int T, int H, int E,
                                                           int E1, float* __restrict__ logits) {
   pdl_launch_dependents();  // let the next kernel on the stream launch early
   pdl_wait();               // inputs written by the previous kernel are visible
@@ -178,9 +178,9 @@ __global__ void __launch_bounds__(256) router_gemv_kernel(const uint8_t* __restr
 // memory and the CTA writes partial logits part[s][t][e]; the top-k kernel
 // adds the splits in order.
 template <int DT>
-__global__ void __launch_bounds__(256) router_mma_kernel(const uint8_t* __restrict__ x,
-                                                         const uint8_t* __restrict__ wr,
-                                                         const uint8_t* __restrict__ swg, int T, int H, int E,
+__global__ void __launch_bounds__(256) router_mma_kernel(const uint8_t* x,
+                                                         const uint8_t* wr,
+                                                         const uint8_t* swg, int T, int H, int E,
                                                          int E1, int cpc, float* __restrict__ part) {
   pdl_launch_dependents();  // let the next kernel on the stream launch early
   pdl_wait();               // inputs written by the previous kernel are visible
@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(256) router_mma_kernel(const uint8_t* __restri
 // (the [T, E1] buffer later kernels read) and ranked from shared memory.
 // One warp per token: rank, weights, outputs.
 template <int MAXM>
-__global__ void __launch_bounds__(256) router_topk_kernel(float* __restrict__ logits, const float* __restrict__ part,
+__global__ void __launch_bounds__(256) router_topk_kernel(float* logits, const float* part,
                                                           int nsplit, int T, int E, int E1, int k, int norm_topk,
                                                           int32_t* ids, float* w, float* logits_out) {
   pdl_launch_dependents();  // let the next kernel on the stream launch early

@@ -16,13 +16,40 @@ struct TcTile {
   int32_t n;     // valid tokens in the tile
 };
 
+// Router logits from its split partial sums part[s][t][e] (flat index
+// q = t * E1 + e, split stride T * E1): v[c] = sum over s, in split order, of
+// part[s][q0 + step * c] for q0 + step * c < limit (0 otherwise), with
+// kSumCols x 8 loads in flight per thread.
+constexpr int kSumCols = 3;
+__device__ __forceinline__ void sum_splits(const float* part, int nsplit, size_t stride, int q0,
+                                           int step, int limit, float (&v)[kSumCols]) {
+#pragma unroll
+  for (int c = 0; c < kSumCols; ++c) v[c] = 0.0f;
+  for (int s0 = 0; s0 < nsplit; s0 += 8) {
+    float pv[kSumCols][8];
+#pragma unroll
+    for (int c = 0; c < kSumCols; ++c)
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int q = q0 + step * c;
+        const bool in = q < limit && s0 + u < nsplit;
+        pv[c][u] = in ? part[static_cast<size_t>(s0 + u) * stride + q] : 0.0f;
+      }
+    // adding +0 for a missing split leaves the sum unchanged (it is never -0)
+#pragma unroll
+    for (int c = 0; c < kSumCols; ++c)
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[c] += pv[c][u];
+  }
+}
+
 // One token's ranking, routing weights and outputs (called by one full warp;
 // s_* are this warp's scratch rows in shared memory).  With nsplit > 0 the
 // logits arrive as nsplit partial sums part[s][t][e] (router_mma_kernel):
 // they are added in split order, stored into `logits` (the [T, E1] buffer
 // later kernels read) and ranked from s_row.
 template <int MAXM>
-__device__ __forceinline__ void topk_token_stage(float* __restrict__ logits, const float* __restrict__ part,
+__device__ __forceinline__ void topk_token_stage(float* logits, const float* part,
                                                  int nsplit, int t, int T, int E, int E1, int k, int norm_topk,
                                                  int32_t* ids, float* w, float* logits_out, int* s_ids,
                                                  float* s_sel, float* s_w, float* s_row) {
@@ -30,11 +57,17 @@ __device__ __forceinline__ void topk_token_stage(float* __restrict__ logits, con
   const float* row = logits + static_cast<size_t>(t) * E1;
   if constexpr (MAXM == 8) {
     if (nsplit > 0) {
-      for (int e = lane; e < E1; e += 32) {
-        float v = 0.0f;
-        for (int sp = 0; sp < nsplit; ++sp) v += part[(static_cast<size_t>(sp) * T + t) * E1 + e];
-        s_row[e] = v;
-        logits[static_cast<size_t>(t) * E1 + e] = v;
+      for (int e0 = lane; e0 < E1; e0 += 32 * kSumCols) {
+        float v[kSumCols];
+        sum_splits(part, nsplit, static_cast<size_t>(T) * E1, t * E1 + e0, 32, t * E1 + E1, v);
+#pragma unroll
+        for (int c = 0; c < kSumCols; ++c) {
+          const int e = e0 + 32 * c;
+          if (e < E1) {
+            s_row[e] = v[c];
+            logits[static_cast<size_t>(t) * E1 + e] = v[c];
+          }
+        }
       }
       __syncwarp();
       row = s_row;
@@ -53,10 +86,11 @@ __device__ __forceinline__ void topk_token_stage(float* __restrict__ logits, con
     for (int e = lane; e < E; e += 32) logits_out[static_cast<size_t>(t) * E + e] = row[e];
 }
 
-__device__ __forceinline__ void group_stage(const int32_t* __restrict__ ids, int T, int k, int E,
+__device__ __forceinline__ void group_stage(const int32_t* ids, int T, int k, int E,
                                                      int has_shared, int32_t* counts_out,
                                                      int32_t* offsets, int32_t* perm, int32_t* tiles,
-                                                     int write_tiles, Control* ctrl) {
+                                                     int write_tiles, Control* ctrl,
+                                                     int32_t* s_counts = nullptr, int32_t* s_offsets = nullptr) {
   __shared__ int32_t cnt[1025 + 1];
   __shared__ int32_t cur[1025 + 1];
   __shared__ int32_t tcnt[1025 + 1];
@@ -116,6 +150,10 @@ __device__ __forceinline__ void group_stage(const int32_t* __restrict__ ids, int
   for (int e = tid; e < n; e += 1024) {
     offsets[e] = cur[e];
     counts_out[e] = cnt[e];
+    if (s_offsets) {  // copies for a later stage of the same CTA
+      s_offsets[e] = cur[e];
+      s_counts[e] = cnt[e];
+    }
   }
   const unsigned long long tot = wtot[31];
   const int n_tiles = static_cast<int>(tot & 0xffffffffu);
@@ -151,8 +189,8 @@ __device__ __forceinline__ void group_stage(const int32_t* __restrict__ ids, int
     for (int t = tid; t < T; t += 1024) perm[cur[E] + t] = np + t;
 }
 
-__device__ __forceinline__ void schedule_stage(const int32_t* __restrict__ counts,
-                                                           const int32_t* __restrict__ offsets, int E, int I,
+__device__ __forceinline__ void schedule_stage(const int32_t* counts,
+                                                           const int32_t* offsets, int E, int I,
                                                            int Is, int H, int N, int mt13, int mt2, int32_t* n13,
                                                            int32_t* n2, TcTile* t13, TcTile* t2) {
   __shared__ unsigned long long wtot[32];
