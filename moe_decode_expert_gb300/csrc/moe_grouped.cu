@@ -220,9 +220,9 @@ moe_status_t launch_grouped(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws,
   const int H = c.hidden, E = c.n_experts, k = c.top_k, I = c.inter, Is = c.shared_inter;
   Control* ctrl = reinterpret_cast<Control*>(ws + L.ctrl);
   const bool use_tc = !(c.flags & MOE_FLAG_GROUPED_SIMT) && L.tc_n > 0 && tc_path_supported(c);
-  // very small batches on the tensor-core path: ranking, grouping and tile lists
-  // in one single-CTA launch (from T = 16 on the multi-CTA ranking is faster)
-  const bool fused = use_tc && T <= 8 && E <= 256;
+  // small batches on the tensor-core path: ranking, grouping and tile lists in
+  // one single-CTA launch, a warp per token
+  const bool fused = use_tc && T <= kRouteGroupMaxT && E <= 256;
   int nsplit = -1;
   if (moe_status_t s = launch_router(c, p.x, p.router_w, p.shared_gate_w, T, p.topk_ids, p.topk_w,
                                      nullptr, ws, L, st, fused ? &nsplit : nullptr))

@@ -682,7 +682,7 @@ __global__ void __launch_bounds__(1024) tc_schedule_kernel(const int32_t* counts
   schedule_stage(counts, offsets, E, I, Is, H, N, mt13, mt2, n13, n2, t13, t2);
 }
 
-// Very small batches (T <= 8, E <= 256): the ranking of every token, the counting
+// Small batches (T <= 32, E <= 256): the ranking of every token, the counting
 // sort of the pairs by expert and the tile lists of both tensor-core passes in
 // one single-CTA launch instead of three (each of those kernels is a few µs of
 // mostly fixed latency at this size).  All 1024 threads add the router's split
@@ -697,12 +697,12 @@ __global__ void __launch_bounds__(1024) route_group_kernel(float* logits, const 
                                                            int32_t* n2, TcTile* t13, TcTile* t2) {
   pdl_launch_dependents();  // let the next kernel on the stream launch early
   pdl_wait();               // inputs written by the previous kernel are visible
-  // T <= 8 and E1 <= 257 (checked on the host)
-  __shared__ float s_lg[8 * 258];  // the T rows of logits
-  __shared__ int s_ids[8][32];
-  __shared__ float s_sel[8][32];
-  __shared__ float s_w[8][32];
-  __shared__ int32_t s_flat[8 * 32];  // ids [T, k]
+  // T <= kRouteGroupMaxT, E1 <= 257, k <= 32 (checked on the host)
+  extern __shared__ float s_lg[];  // the T rows of logits [T, E1] (dynamic)
+  __shared__ int s_ids[kRouteGroupMaxT][32];
+  __shared__ float s_sel[kRouteGroupMaxT][32];
+  __shared__ float s_w[kRouteGroupMaxT][32];
+  __shared__ int32_t s_flat[kRouteGroupMaxT * 32];  // ids [T, k]
   __shared__ int32_t s_cnt[258], s_off[258];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // The logits: the router's split partial sums added by every thread (all
@@ -850,7 +850,9 @@ static moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uin
   if (fused_nsplit >= 0) {  // ranking + grouping + tile lists in one launch (small batches)
     float* lg = reinterpret_cast<float*>(ws + L.r_logits);
     const int E1 = c.has_shared_gate ? E + 1 : E;
-    launch_pdl(route_group_kernel, dim3(1), dim3(1024), 0, st, lg, reinterpret_cast<const float*>(ws + L.r_part),
+    const size_t lg_bytes = static_cast<size_t>(T) * E1 * sizeof(float);
+    cudaFuncSetAttribute(route_group_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(lg_bytes));
+    launch_pdl(route_group_kernel, dim3(1), dim3(1024), lg_bytes, st, lg, reinterpret_cast<const float*>(ws + L.r_part),
                fused_nsplit, T, E, E1, k, c.norm_topk, p.topk_ids, p.topk_w, Is > 0 ? 1 : 0, counts, offsets, perm,
                ctrl, I, Is, H, N, mt13, kMT, sched, sched + 1, t13, t2);
     if (moe_status_t s = check_launch("route_group_kernel")) return s;

@@ -8,6 +8,7 @@
 namespace moe {
 
 constexpr int kTN = 8;  // pairs (tokens) per tile of the CUDA-core grouped kernels
+constexpr int kRouteGroupMaxT = 32;  // tokens of the single-CTA ranking + grouping kernel (a warp each)
 
 struct TcTile {
   int32_t e;     // expert id, E = shared expert
