@@ -263,6 +263,7 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
   __shared__ uint32_t s_fail;
   __shared__ int s_next;                // next phase-3 work item of this CTA
   __shared__ unsigned long long s_cand[64];  // per-warp top-k candidates (64-bit rank keys)
+  __shared__ __align__(16) unsigned long long s_wkey[256];  // every logit's 64-bit rank key
   __shared__ volatile int s_wready;     // routing weights and gate are in s_w / s_gate
   __shared__ float s_red[kDecWarps][64];
 
@@ -431,11 +432,11 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
   }
 
   // ---- phase 2: the logits, their top-k (fp32, lower index first on ties)
-  // and the routing weights.  Warp w reads logits 32w..32w+31 (one exchange
-  // word per lane; the gate logit rides along at index E) and keeps its own
-  // top-k by k rounds of warp max + lowest lane; the 8 warps' candidates are
-  // then ranked exactly by all threads (4 threads per candidate, 64-bit keys
-  // (logit key, ~index) are unique), and candidate rank r < k fills slot r.
+  // and the routing weights.  Every logit gets a unique 64-bit key (logit
+  // key, ~index).  Lane l of warp w counts how many of logits 32w..32w+31 have
+  // a larger key (16 broadcast shared loads); ranks below k are the warp's
+  // candidates.  The 8 warps' candidates are then ranked exactly by all
+  // threads (4 threads per candidate), and candidate rank r < k fills slot r.
   if (E <= 256 && k <= 8) {
     if (warp == 0) {  // one warp polls the words (all warps polling floods L2)
       const uint64_t* src = a.ll_logits + static_cast<size_t>(cta % kLogitReplicas) * a.ll_stride;
@@ -445,16 +446,21 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
     __syncthreads();
     const int i0 = warp * 32 + lane;
     const float v0 = lg[min(i0, E - 1)];              // clamped load, no branch
-    uint32_t key = i0 < E ? order_key(v0) : 0u;       // finite logits have keys > 0
-    uint64_t mine = 0;
-    for (int r = 0; r < k; ++r) {
-      const uint32_t m = __reduce_max_sync(0xffffffffu, key);
-      const uint32_t b = __ballot_sync(0xffffffffu, key == m && key != 0u);
-      const int wl = __ffs(b) - 1;
-      mine = (lane == r && b) ? (static_cast<uint64_t>(m) << 32) | static_cast<uint32_t>(~(warp * 32 + wl)) : mine;
-      key = lane == wl ? 0u : key;
+    const uint32_t key = i0 < E ? order_key(v0) : 0u;  // finite logits have keys > 0
+    // unique 64-bit key (logit key, ~index): its rank among the warp's 32 is
+    // the number of larger keys; ranks below k are the warp's candidates
+    const uint64_t mk = key ? (static_cast<uint64_t>(key) << 32) | static_cast<uint32_t>(~i0) : 0ull;
+    s_wkey[i0] = mk;
+    if (lane < 8) s_cand[warp * 8 + lane] = 0ull;
+    __syncwarp();
+    int rk = 0;
+    const ulonglong2* wk = reinterpret_cast<const ulonglong2*>(s_wkey + warp * 32);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const ulonglong2 kk = wk[j];  // same address in every lane: broadcast
+      rk += (kk.x > mk ? 1 : 0) + (kk.y > mk ? 1 : 0);
     }
-    if (lane < 8) s_cand[warp * 8 + lane] = mine;
+    if (mk != 0ull && rk < k) s_cand[warp * 8 + rk] = mk;
     __syncthreads();
     {
       const int c = tid >> 2, q4 = tid & 3;

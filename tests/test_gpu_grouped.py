@@ -61,6 +61,25 @@ def test_small_batch_zipf(m, T, flags):
     _check_tokens(ids, w, out, ref, tokens, wl.top_k)
 
 
+@pytest.mark.parametrize("T", [9, 31, 32, 33])
+def test_small_batch_fused_ranking_boundary(m, T):
+    """Up to 32 tokens one single-CTA launch ranks (a warp per token), groups
+    and lists the tiles; from 33 on the ranking, grouping and tile lists are
+    three launches.  Both sides of the boundary, and ragged counts, match the
+    oracle."""
+    wl = moe_synth.workload("small_batch")
+    g = moe_synth.make_layer(wl, 2, T, device=DEV)
+    m.moe_reset_stats()
+    ids, w, out = _grouped(m, wl, g, T, flags=TC)
+    st = m.moe_get_stats()
+    assert st["grouped_tc_calls"] == 1
+    assert st["kernels_launched"] == (6 if T <= 32 else 8)
+    picks = np.random.default_rng(T).choice(T, 6, replace=False).tolist()
+    tokens = sorted(set([0, T - 1] + picks))
+    ref = oracle_sampled(wl, g, tokens)
+    _check_tokens(ids, w, out, ref, tokens, wl.top_k)
+
+
 @pytest.mark.parametrize("flags", [SIMT, TC], ids=["simt", "tcgen05"])
 @pytest.mark.parametrize("T", [3, 65, 130])
 def test_odd_token_counts_small_shapes(m, T, flags):
