@@ -155,12 +155,13 @@ __device__ __forceinline__ bool epi_any(bool v) {
 // one expert share every token (B) stage, so the token operand is read from L2
 // once per MT M-tiles; each tile has its own TMEM accumulator (2*MT*N columns
 // with double buffering).
-template <int DT, int N, int MT>
+template <int DT, int N, int MT, bool DIRECT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_w13_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapAs,
                   const __grid_constant__ CUtensorMap mapB, const TcTile* tiles,
                   const int32_t* n_tiles_p, int H, int I, int Is, int E, int act_stride,
-                  uint16_t* __restrict__ act_hi, uint16_t* __restrict__ act_lo, Control* ctrl, uint64_t timeout) {
+                  uint16_t* __restrict__ act_hi, uint16_t* __restrict__ act_lo, Control* ctrl, uint64_t timeout,
+                  const int32_t* perm, int direct_T, int k) {
   pdl_launch_dependents();  // let the next kernel on the stream launch early
   constexpr uint32_t kStage = MT * kTileA + N * 128;
   constexpr int kStg = 128 * 17 * 4;
@@ -172,6 +173,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __shared__ __align__(8) uint64_t full[kStages], empty[kStages], tfull[2], tempty[2], done;
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int s_abort;
+  __shared__ int s_tok[DIRECT ? N : 1];  // DIRECT: token of each pair of the current tile
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -224,7 +226,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tma_load_2d(sA + mt * kTileA, mA, &full[stage], kb * kBK, rowg + mt * 64);
             tma_load_2d(sA + mt * kTileA + kTileA / 2, mA, &full[stage], kb * kBK, rowg + mt * 64 + ie);
           }
-          tma_load_2d(sA + MT * kTileA, &mapB, &full[stage], kb * kBK, tl.pos0);
+          tma_load_2d(sA + MT * kTileA, &mapB, &full[stage], kb * kBK, DIRECT ? 0 : tl.pos0);
           issued_mask |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -291,6 +293,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int ie = tl.e == E ? Is : I;
       const int nv = min(MT, ie / 64 - tl.m * MT);
       const int acc = it & 1;
+      if constexpr (DIRECT)  // token (accumulator column) of each pair of the tile
+        for (int c = etid; c < tl.n; c += 128) {
+          const int p = perm[tl.pos0 + c];
+          s_tok[c] = p < direct_T * k ? p / k : p - direct_T * k;
+        }
       const bool ok = !s_abort && tc_wait(&tfull[acc], (it >> 1) & 1, timeout, &s_abort);
       if (epi_any(!ok)) {
         s_abort = 1;
@@ -300,20 +307,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_after();
       for (int mt = 0; mt < nv; ++mt) {
         const int i = (tl.m * MT + mt) * 64 + ar;
-        for (int c0 = 0; c0 < tl.n; c0 += 16) {
+        const int ncols = DIRECT ? direct_T : tl.n;  // accumulator columns holding results
+        for (int c0 = 0; c0 < ncols; c0 += 16) {
           float v[16];
           tmem_ld16(tbase + (static_cast<uint32_t>(32 * q) << 16) +
                         static_cast<uint32_t>((acc * MT + mt) * N + c0), v);
 #pragma unroll
           for (int j = 0; j < 16; ++j) stg[row * 17 + j] = v[j];
           named_bar_sync(1, 128);
+          if constexpr (DIRECT) {
+            // column = token: pair j of the tile takes its token's column
+            for (int j = half; j < tl.n; j += 2) {
+              const int col = s_tok[j] - c0;
+              if (col >= 0 && col < 16) {
+                const float g = stg[ar * 17 + col], u = stg[(ar + 64) * 17 + col];
+                split_store<DT>(act_hi, act_lo, static_cast<size_t>(tl.pos0 + j) * act_stride + i, silu_f(g) * u);
+              }
+            }
+          } else {
 #pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
-            const int j = half * 8 + jj;
-            const int col = c0 + j;
-            if (col < tl.n) {
-              const float g = stg[ar * 17 + j], u = stg[(ar + 64) * 17 + j];
-              split_store<DT>(act_hi, act_lo, static_cast<size_t>(tl.pos0 + col) * act_stride + i, silu_f(g) * u);
+            for (int jj = 0; jj < 8; ++jj) {
+              const int j = half * 8 + jj;
+              const int col = c0 + j;
+              if (col < tl.n) {
+                const float g = stg[ar * 17 + j], u = stg[(ar + 64) * 17 + j];
+                split_store<DT>(act_hi, act_lo, static_cast<size_t>(tl.pos0 + col) * act_stride + i, silu_f(g) * u);
+              }
             }
           }
           named_bar_sync(1, 128);
@@ -862,9 +881,17 @@ static moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uin
     if (moe_status_t s = check_launch("tc_schedule_kernel")) return s;
   }
   const int sms = sm_count();
-  const int gg = (P + 7) / 8 < sms * 8 ? (P + 7) / 8 : sms * 8;
-  launch_pdl(tc_gather_kernel, dim3(gg), dim3(256), 0, st, static_cast<const uint8_t*>(p.x), perm, P, T, k, H, xs);
-  if (moe_status_t s = check_launch("tc_gather_kernel")) return s;
+  // Up to 16 tokens the W13 pass reads x itself (B = all T tokens, each pair
+  // takes its token's accumulator column) and the gather of x rows into expert
+  // order is not needed (T = 2 / 8 / 16: about 2 us less per layer).  With
+  // more tokens every CTA reads the same x rows at the same time (8 KB per
+  // stage at T = 64, +10 us per layer), so the gathered rows are used.
+  const bool direct = T <= 16 && T <= N;
+  if (!direct) {
+    const int gg = (P + 7) / 8 < sms * 8 ? (P + 7) / 8 : sms * 8;
+    launch_pdl(tc_gather_kernel, dim3(gg), dim3(256), 0, st, static_cast<const uint8_t*>(p.x), perm, P, T, k, H, xs);
+    if (moe_status_t s = check_launch("tc_gather_kernel")) return s;
+  }
 
   CUtensorMap mA, mAs, mB, mW2, mW2s, mHi, mLo, mHiS, mLoS;
   const void* sw13 = p.shared_w13 ? p.shared_w13 : p.w13;
@@ -872,7 +899,8 @@ static moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uin
   const int IsM = Is > 0 ? Is : I;
   bool ok = make_map(&mA, DT, p.w13, H, static_cast<uint64_t>(E) * 2 * I, static_cast<uint64_t>(H) * 2, 64) &&
             make_map(&mAs, DT, sw13, H, 2ull * IsM, static_cast<uint64_t>(H) * 2, 64) &&
-            make_map(&mB, DT, xs, H, P, static_cast<uint64_t>(H) * 2, N) &&
+            (direct ? make_map(&mB, DT, p.x, H, T, static_cast<uint64_t>(H) * 2, N)
+                    : make_map(&mB, DT, xs, H, P, static_cast<uint64_t>(H) * 2, N)) &&
             make_map(&mW2, DT, p.w2, I, static_cast<uint64_t>(E) * H, static_cast<uint64_t>(I) * 2, 128) &&
             make_map(&mW2s, DT, sw2, IsM, H, static_cast<uint64_t>(IsM) * 2, 128) &&
             make_map(&mHi, DT, ahi, I, P, static_cast<uint64_t>(Imax) * 2, N) &&
@@ -885,16 +913,17 @@ static moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uin
   cudaFuncSetAttribute(tc_w2_kernel<DT, N, kMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s2));
   const int g13 = static_cast<int>(L.tc_max13 < sms ? L.tc_max13 : sms);
   const int g2 = static_cast<int>(L.tc_max2 < sms ? L.tc_max2 : sms);
+  auto launch13 = [&](auto kernel, size_t s13) {
+    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s13));
+    launch_pdl(kernel, dim3(g13 > 0 ? g13 : 1), dim3(kTcThreads), s13, st, mA, mAs, mB, t13, sched, H, I, Is, E,
+               Imax, ahi, alo, ctrl, timeout, perm, direct ? T : 0, k);
+  };
   if (mt13 == 1) {
-    const size_t s13 = tc_smem13<N, 1>();
-    cudaFuncSetAttribute(tc_w13_kernel<DT, N, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s13));
-    launch_pdl(tc_w13_kernel<DT, N, 1>, dim3(g13 > 0 ? g13 : 1), dim3(kTcThreads), s13, st, mA, mAs, mB, t13, sched, H,
-               I, Is, E, Imax, ahi, alo, ctrl, timeout);
+    if (direct) launch13(tc_w13_kernel<DT, N, 1, true>, tc_smem13<N, 1>());
+    else launch13(tc_w13_kernel<DT, N, 1, false>, tc_smem13<N, 1>());
   } else {
-    const size_t s13 = tc_smem13<N, kMT>();
-    cudaFuncSetAttribute(tc_w13_kernel<DT, N, kMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s13));
-    launch_pdl(tc_w13_kernel<DT, N, kMT>, dim3(g13 > 0 ? g13 : 1), dim3(kTcThreads), s13, st, mA, mAs, mB, t13, sched,
-               H, I, Is, E, Imax, ahi, alo, ctrl, timeout);
+    if (direct) launch13(tc_w13_kernel<DT, N, kMT, true>, tc_smem13<N, kMT>());
+    else launch13(tc_w13_kernel<DT, N, kMT, false>, tc_smem13<N, kMT>());
   }
   if (moe_status_t s = check_launch("tc_w13_kernel")) return s;
   launch_pdl(tc_w2_kernel<DT, N, kMT>, dim3(g2 > 0 ? g2 : 1), dim3(kTcThreads), s2, st, mW2, mW2s, mHi, mLo, mHiS, mLoS, t2, sched + 1,
@@ -902,7 +931,7 @@ static moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uin
                                                                    c.has_shared_gate, T, H, I, Is, E, k, y, ctrl,
                                                                    timeout);
   if (moe_status_t s = check_launch("tc_w2_kernel")) return s;
-  stat_kernels(4);
+  stat_kernels(direct ? 3 : 4);
   return MOE_OK;
 }
 

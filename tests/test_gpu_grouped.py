@@ -61,11 +61,12 @@ def test_small_batch_zipf(m, T, flags):
     _check_tokens(ids, w, out, ref, tokens, wl.top_k)
 
 
-@pytest.mark.parametrize("T", [9, 31, 32, 33])
+@pytest.mark.parametrize("T", [9, 16, 17, 31, 32, 33])
 def test_small_batch_fused_ranking_boundary(m, T):
     """Up to 32 tokens one single-CTA launch ranks (a warp per token), groups
     and lists the tiles; from 33 on the ranking, grouping and tile lists are
-    three launches.  Both sides of the boundary, and ragged counts, match the
+    three launches.  Up to 16 tokens the W13 pass reads x itself (no gather
+    launch).  Both sides of the boundaries, and ragged counts, match the
     oracle."""
     wl = moe_synth.workload("small_batch")
     g = moe_synth.make_layer(wl, 2, T, device=DEV)
@@ -73,7 +74,10 @@ def test_small_batch_fused_ranking_boundary(m, T):
     ids, w, out = _grouped(m, wl, g, T, flags=TC)
     st = m.moe_get_stats()
     assert st["grouped_tc_calls"] == 1
-    assert st["kernels_launched"] == (6 if T <= 32 else 8)
+    # router (+ top-k), ranking/grouping/tile lists (1 or 3), gather (0 or 1),
+    # W13, W2, combine
+    expect = (1 + 1 if T <= 32 else 2 + 2) + (0 if T <= 16 else 1) + 3
+    assert st["kernels_launched"] == expect
     picks = np.random.default_rng(T).choice(T, 6, replace=False).tolist()
     tokens = sorted(set([0, T - 1] + picks))
     ref = oracle_sampled(wl, g, tokens)
