@@ -8,7 +8,8 @@
 // real matrix product.  Swap-AB formulation per expert e with m_e tokens:
 //
 //   W13 pass   D[128 rows, N tokens] = [Wg rows i0..i0+63 ; Wu rows i0..i0+63] . Xs^T
-//              (K = H), epilogue act = silu(gate) * up for the 64 rows, stored as
+//              (K = H; Xs = x rows in expert order, or x itself for T <= 16),
+//              epilogue act = silu(gate) * up for the 64 rows, stored as
 //              a two-term split act = hi + lo in the storage dtype (hi = rn(act),
 //              lo = rn(act - hi): 16 significant bits) so the next pass keeps
 //              fp32-level accuracy of the activation;
@@ -154,7 +155,10 @@ __device__ __forceinline__ bool epi_any(bool v) {
 // MT 128-row M-tiles (each 64 gate rows stacked on the matching 64 up rows) of
 // one expert share every token (B) stage, so the token operand is read from L2
 // once per MT M-tiles; each tile has its own TMEM accumulator (2*MT*N columns
-// with double buffering).
+// with double buffering).  The token operand is the gathered rows Xs (rows
+// pos0.. of the tile's pairs), or with DIRECT (T <= 16) x itself: every tile
+// then computes all T token columns and pair j of the tile takes the column of
+// its token.
 template <int DT, int N, int MT, bool DIRECT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_w13_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapAs,
