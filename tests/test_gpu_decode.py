@@ -171,6 +171,7 @@ def test_duplicated_router_rows_rank_lower_index_first(m):
     (512, 8, 32, 0, 0, moe_synth.F16, 1),
     (64, 6, 48, 16, 0, moe_synth.BF16, 0),
     (1024, 32, 16, 8, 1, moe_synth.F16, 1),
+    (320, 8, 200, 64, 1, moe_synth.BF16, 1),  # two pairs in flight per warp, general ranking and combine
 ])
 def test_shape_variants(m, E, k, I, Is, gate, dt, norm):
     wl = moe_synth.Workload("v", 512, E, k, I, Is, dt, gate, 1.0, 0.05, 0.05, norm_topk=norm, preset_id=9)
