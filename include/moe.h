@@ -60,7 +60,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 1
+#define MOE_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define MOE_API __attribute__((visibility("default")))
@@ -126,6 +126,8 @@ typedef struct moe_stats {
   uint64_t grouped_calls;        /* T > 1 grouped path (either kind)            */
   uint64_t grouped_tc_calls;     /* ... of which on the tcgen05 kernels         */
   uint64_t kernels_launched;     /* every kernel this library enqueued          */
+  uint64_t decode_general_calls; /* T == 1 calls on the all-paths decode kernel
+                                    (shapes outside the specialised ones)       */
 } moe_stats_t;
 
 /* ABI version of the loaded library (MOE_ABI_VERSION it was built with). */

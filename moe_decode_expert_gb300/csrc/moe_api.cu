@@ -30,8 +30,10 @@ moe_status_t check_launch(const char* what) {
 }
 
 // ---------------------------------------------------------------- counters
-static std::atomic<uint64_t> g_decode{0}, g_router{0}, g_grouped{0}, g_grouped_tc{0}, g_kernels{0};
+static std::atomic<uint64_t> g_decode{0}, g_router{0}, g_grouped{0}, g_grouped_tc{0}, g_kernels{0},
+    g_decode_general{0};
 void stat_decode() { g_decode.fetch_add(1, std::memory_order_relaxed); }
+void stat_decode_general() { g_decode_general.fetch_add(1, std::memory_order_relaxed); }
 void stat_router() { g_router.fetch_add(1, std::memory_order_relaxed); }
 void stat_grouped() { g_grouped.fetch_add(1, std::memory_order_relaxed); }
 void stat_grouped_tc() { g_grouped_tc.fetch_add(1, std::memory_order_relaxed); }
@@ -308,6 +310,7 @@ moe_status_t moe_get_stats(moe_stats_t* stats) {
   stats->grouped_calls = g_grouped.load();
   stats->grouped_tc_calls = g_grouped_tc.load();
   stats->kernels_launched = g_kernels.load();
+  stats->decode_general_calls = g_decode_general.load();
   return MOE_OK;
 }
 
@@ -317,6 +320,7 @@ void moe_reset_stats(void) {
   g_grouped = 0;
   g_grouped_tc = 0;
   g_kernels = 0;
+  g_decode_general = 0;
 }
 
 moe_status_t moe_set_wait_timeout_ns(uint64_t ns) {

@@ -907,6 +907,7 @@ moe_status_t launch_decode_fused(const moe_cfg_t& c, const BlockPtrs& p, uint8_t
                         c.inter % 16 == 0 && c.shared_inter % 16 == 0;
   const int kpw = ((K + 15) / 16 + kDecWarps - 1) / kDecWarps;  // 16-column steps per warp
   const int mode = !standard ? kDecGeneral : ((kpw * 16 + 1) / 2 <= 4 * 32 ? kDecNarrow : kDecWide);
+  if (mode == kDecGeneral) stat_decode_general();
   auto go = [&](auto dt, auto depth) -> moe_status_t {
     constexpr int D = decltype(dt)::value, P = decltype(depth)::value;
     if (mode == kDecNarrow) return launch_decode_dt<D, P, kDecNarrow>(a, G, smem, st);

@@ -57,6 +57,7 @@ moe_status_t check_launch(const char* what);
 
 // Process-wide counters.
 void stat_decode();
+void stat_decode_general();
 void stat_router();
 void stat_grouped();
 void stat_grouped_tc();

@@ -46,6 +46,7 @@ def test_library_is_the_native_path(m):
     _decode(m, wl, _to(moe_synth.make_layer(wl, 0, 1)))
     st = m.moe_get_stats()
     assert st["decode_fused_calls"] == 1 and st["kernels_launched"] == 1
+    assert st["decode_general_calls"] == 0  # a standard shape: the specialised kernel
     maps = open("/proc/self/maps").read()
     assert "libmoe_gb300.so" in maps
 
@@ -175,15 +176,23 @@ def test_duplicated_router_rows_rank_lower_index_first(m):
 ])
 def test_shape_variants(m, E, k, I, Is, gate, dt, norm):
     wl = moe_synth.Workload("v", 512, E, k, I, Is, dt, gate, 1.0, 0.05, 0.05, norm_topk=norm, preset_id=9)
+    # the launch takes the specialised kernel only for the standard shapes
+    H = 512
+    G = min(torch.cuda.get_device_properties(0).multi_processor_count, k * I)
+    standard = E <= 256 and k <= 8 and H >= G and -(-H // G) <= 16 and I % 16 == 0 and Is % 16 == 0
+    m.moe_reset_stats()
+    calls = 0
     for layer in range(2):
         d = moe_synth.make_layer(wl, layer, 1)
         ref = oracle_full(wl, d)
         if min_rank_gap(ref["logits"], k)[0] < 1e-5:
             continue
         ids, w, out = _decode(m, wl, _to(d), out_dtype=3)
+        calls += 1
         assert np.array_equal(ids.cpu().numpy(), ref["ids"])
         np.testing.assert_allclose(w.cpu().numpy(), ref["w"], rtol=1e-5, atol=1e-7)
         parity(out, ref["out"])
+    assert m.moe_get_stats()["decode_general_calls"] == (0 if standard else calls)
 
 
 def test_repeated_calls_share_one_workspace(m):
