@@ -378,9 +378,12 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
   bool va, vb;
   const uint8_t* ra = p1_row(g, va);
   const uint8_t* rb = p1_row(g + 8, vb);
+  // With DEPTH 2 (one CTA per SM, so a CTA starts only when its SM frees up)
+  // the shared expert's W2 copies go out in phase 3 with the routed ones,
+  // keeping the work before the wait short (full-width layer 20.08 -> 19.75 us).
   if (a.static_weights) {
     gv.issue(ra, va, rb, vb, c0w, cb1, t);
-    if (Is > 0) copy_w2_cols(true);
+    if (DEPTH == 1 && Is > 0) copy_w2_cols(true);
   }
   pdl_wait();  // x (and anything else an earlier kernel wrote) is visible from here
   if (!a.static_weights) gv.issue(ra, va, rb, vb, c0w, cb1, t);
@@ -402,7 +405,7 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
     // launch, which has completed; clear it for the next launch.
     if (cta == 0) atomicExch(&a.ctrl->arrive[(s_epoch + 1u) & 1u], 0u);
   }
-  if (!a.static_weights && Is > 0) copy_w2_cols(true);
+  if (DEPTH == 1 && !a.static_weights && Is > 0) copy_w2_cols(true);
   __syncthreads();
   const uint32_t epoch = s_epoch;
 
@@ -604,12 +607,19 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
         if (pa >= P) break;
         start_pair(rp, pa);
         if (pb < P) start_pair(rq, pb);
-        if (!copied) { copy_w2_cols(false); copied = true; }
+        if (!copied) {
+          if (Is > 0) copy_w2_cols(true);
+          copy_w2_cols(false);
+          copied = true;
+        }
         if (!end_pair(rp, pa) || pb >= P) break;
         if (!end_pair(rq, pb)) break;
       }
     }
-    if (!copied) copy_w2_cols(false);
+    if (!copied) {
+      if (Is > 0) copy_w2_cols(true);
+      copy_w2_cols(false);
+    }
   }
 
   // ---- phase 4 (per warp): this warp's activations and W2 columns
