@@ -263,24 +263,24 @@ moe_status_t launch_grouped(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws,
     const int g2 = static_cast<int>(items2 < sms * 8LL ? items2 : sms * 8LL);
     const uint8_t* x = static_cast<const uint8_t*>(p.x);
     if (c.dtype == MOE_BF16) {
-      cudaFuncSetAttribute(grouped_w13_kernel<MOE_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem13);
+      raise_smem_limit(grouped_w13_kernel<MOE_BF16>, smem13);
       launch_pdl(grouped_w13_kernel<MOE_BF16>, dim3(g13), dim3(kGThreads), smem13, st, 
           x, static_cast<const uint8_t*>(p.w13), static_cast<const uint8_t*>(p.shared_w13), counts, offsets,
           perm, tiles, T, H, E, k, I, Is, Imax, act);
     } else {
-      cudaFuncSetAttribute(grouped_w13_kernel<MOE_F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem13);
+      raise_smem_limit(grouped_w13_kernel<MOE_F16>, smem13);
       launch_pdl(grouped_w13_kernel<MOE_F16>, dim3(g13), dim3(kGThreads), smem13, st, 
           x, static_cast<const uint8_t*>(p.w13), static_cast<const uint8_t*>(p.shared_w13), counts, offsets,
           perm, tiles, T, H, E, k, I, Is, Imax, act);
     }
     if (moe_status_t s = check_launch("grouped_w13_kernel")) return s;
     if (c.dtype == MOE_BF16) {
-      cudaFuncSetAttribute(grouped_w2_kernel<MOE_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
+      raise_smem_limit(grouped_w2_kernel<MOE_BF16>, smem2);
       launch_pdl(grouped_w2_kernel<MOE_BF16>, dim3(g2), dim3(kGThreads), smem2, st, 
           static_cast<const uint8_t*>(p.w2), static_cast<const uint8_t*>(p.shared_w2), counts, offsets, perm,
           tiles, p.topk_w, glog, gate_stride, c.has_shared_gate, T, H, E, k, I, Is, Imax, act, y);
     } else {
-      cudaFuncSetAttribute(grouped_w2_kernel<MOE_F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
+      raise_smem_limit(grouped_w2_kernel<MOE_F16>, smem2);
       launch_pdl(grouped_w2_kernel<MOE_F16>, dim3(g2), dim3(kGThreads), smem2, st, 
           static_cast<const uint8_t*>(p.w2), static_cast<const uint8_t*>(p.shared_w2), counts, offsets, perm,
           tiles, p.topk_w, glog, gate_stride, c.has_shared_gate, T, H, E, k, I, Is, Imax, act, y);

@@ -874,7 +874,7 @@ static moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uin
     float* lg = reinterpret_cast<float*>(ws + L.r_logits);
     const int E1 = c.has_shared_gate ? E + 1 : E;
     const size_t lg_bytes = static_cast<size_t>(T) * E1 * sizeof(float);
-    cudaFuncSetAttribute(route_group_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(lg_bytes));
+    if (raise_smem_limit(route_group_kernel, lg_bytes) != cudaSuccess) return check_launch("route_group_kernel (smem)");
     launch_pdl(route_group_kernel, dim3(1), dim3(1024), lg_bytes, st, lg, reinterpret_cast<const float*>(ws + L.r_part),
                fused_nsplit, T, E, E1, k, c.norm_topk, p.topk_ids, p.topk_w, Is > 0 ? 1 : 0, counts, offsets, perm,
                ctrl, I, Is, H, N, mt13, kMT, sched, sched + 1, t13, t2);

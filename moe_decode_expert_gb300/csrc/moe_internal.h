@@ -108,6 +108,18 @@ moe_status_t launch_tc_router(const moe_cfg_t& c, const void* x, const void* rou
 moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws, const WsLayout& L, int32_t T,
                               int fused_nsplit, cudaStream_t st);
 
+// Raise, never lower, a kernel's dynamic shared-memory limit on the current
+// device: a graph captured with a larger launch still runs after a call that
+// needed less.
+template <typename K>
+inline cudaError_t raise_smem_limit(K kernel, size_t bytes) {
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
+  if (e != cudaSuccess) return e;
+  if (static_cast<size_t>(fa.maxDynamicSharedSizeBytes) >= bytes) return cudaSuccess;
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+}
+
 // Launch with programmatic stream serialization: the kernel may be scheduled
 // while the previous kernel on the stream drains.  Every kernel of the library
 // runs griddepcontrol.wait before it reads anything an earlier kernel may

@@ -159,3 +159,38 @@ def test_simt_and_tcgen05_paths_agree(m):
     i2, w2, o2 = _grouped(m, wl, g, T, out_dtype=3, flags=TC)
     assert torch.equal(i1, i2) and torch.equal(w1, w2)
     parity(o2, o1.double().cpu().numpy(), max_err_frac=1e-3, rel_l1=1e-4)
+
+
+def test_graph_replays_after_a_smaller_call(m):
+    """A CUDA graph captured at T = 16 still launches, with the same result,
+    after an eager call at T = 2 on the same path (kernel shared-memory limits
+    are raised, never lowered)."""
+    wl = moe_synth.workload("small_batch")
+    g16 = moe_synth.make_layer(wl, 3, 16, device=DEV)
+    g2 = moe_synth.make_layer(wl, 4, 2, device=DEV)
+    cfg = m.cfg_from_workload(wl, None, TC)
+    ids = torch.empty(16, wl.top_k, dtype=torch.int32, device=DEV)
+    w = torch.empty(16, wl.top_k, dtype=torch.float32, device=DEV)
+    out = torch.empty(16, wl.hidden, dtype=cfg.out_torch_dtype, device=DEV)
+    ws = m.alloc_workspace(cfg, 16, DEV)
+    st = torch.cuda.Stream(device=DEV)
+    st.wait_stream(torch.cuda.current_stream(DEV))
+
+    def call():
+        m.moe_grouped_forward(cfg, g16["x"], g16["router_w"], g16["w13"], g16["w2"], g16["shared_w13"],
+                              g16["shared_w2"], g16["shared_gate_w"], ids, w, out, ws, st)
+
+    with torch.cuda.stream(st):
+        call()
+    torch.cuda.synchronize()
+    eager = out.clone()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=st):
+        call()
+    _grouped(m, wl, g2, 2, flags=TC)  # a smaller call in between
+    out.zero_()
+    with torch.cuda.stream(st):
+        graph.replay()
+    torch.cuda.synchronize()
+    m.moe_query_status(ws)
+    assert torch.equal(out, eager)
