@@ -64,3 +64,15 @@ def test_grouped_bytes_model():
     expect = 2 * (E * H + 10 * 3 * I * H + 3 * Is * H + H) + 2 * 2 * 4 * H
     assert bench.grouped_bytes(wl, 4, 10) == expect
     assert bench.grouped_flops(wl, 1) == 2 * (E * H + 8 * 3 * I * H + 3 * Is * H)
+
+
+def test_kernel_code_hash_ignores_comments_only():
+    """The committed ncu traffic stays valid across comment edits of the
+    kernel sources, and is dropped when their code changes."""
+    src = 'int f() {  // first\n  return g("a//b");  // the string keeps its slashes\n}\n// trailing note\n'
+    same = 'int f() {  // reworded\n\n  return g("a//b");\n}\n'
+    changed = 'int f() {  // first\n  return g("a//c");\n}\n'
+    h = lambda text: bench.kernel_source_hash(lambda f: text)
+    assert bench.code_lines(src) == ['int f() {', '  return g("a//b");', '}']
+    assert h(src) == h(same)
+    assert h(src) != h(changed)
