@@ -93,6 +93,62 @@ def test_known_data_w2_gives_128(dtype):
     assert not np.any(out == g["wrong_value_reported"])
 
 
+# ------------------------------------- W2 layout [E, H, I] on random activations
+def _rank1_w2(E, H, I, dtype, rng):
+    """W2[e, h, i] = s_e * a_h * b_i with small dyadic factors, exact in fp16
+    and bf16 (each product has at most 7 significant bits)."""
+    a = 1 + rng.integers(0, 4, H) / 4
+    b = 1 + rng.integers(0, 8, I) / 8
+    s = 2.0 ** rng.integers(-2, 3, E)
+    w = s[:, None, None] * a[None, :, None] * b[None, None, :]
+    bits = _bits_of(w, dtype)
+    assert np.array_equal(_to64(bits, dtype), w)
+    return bits, a, b, s
+
+
+@pytest.mark.parametrize("dtype", [F16, BF16])
+def test_w2_combine_rank_one_w2_on_random_activations(dtype):
+    """The down projection reads row h of expert e as the I contiguous values
+    W2[e, h, 0:I] (work log Parts 4 and 10: W2[expert_ids[k], h, :]).  With
+    a rank-one W2 = s_e a_h b_i the routed output is a_h times one scalar,
+    sum_j w_j s_{id_j} sum_i b_i act[j, i], for any activation.  A transposed
+    or shifted index (H != I here) breaks the proportionality."""
+    rng = np.random.default_rng(11)
+    H, I, E, k = 40, 24, 6, 3
+    cfg = OracleCfg(hidden=H, n_experts=E, top_k=k, inter=I, dtype=dtype)
+    w2, a, b, s = _rank1_w2(E, H, I, dtype, rng)
+    act = rng.standard_normal((k, I))
+    ids = rng.permutation(E)[:k].astype(np.int32)
+    w = rng.random(k) + 0.1
+    out = oracle.w2_combine(cfg, act, ids, w, w2)
+    scalar = sum(w[j] * s[ids[j]] * float(np.dot(b, act[j])) for j in range(k))
+    np.testing.assert_allclose(out, a * scalar, rtol=1e-12, atol=0)
+
+
+@pytest.mark.parametrize("dtype", [F16, BF16])
+@pytest.mark.parametrize("Is,gate", [(0, 0), (16, 1)])
+def test_forward_rank_one_w2_output_is_proportional(dtype, Is, gate):
+    """Whole block on random x, router and W13 with rank-one down projections
+    (routed W2[e, h, i] = s_e a_h b_i, shared Ws2[h, i] = a_h c_i): every
+    token's output is a_h times a per-token scalar, whatever the routing and
+    the activations.  Pins the [E, H, I] and [H, Is] layouts of the forward
+    pass on random data (the closed-form tests use W2 = 1, which any index
+    order satisfies)."""
+    rng = np.random.default_rng(12)
+    H, E, k, I, T = 40, 8, 3, 24, 3
+    d = _rand_case(rng, H, E, k, I, Is, dtype, gate, T)
+    d["w2"], a, b, s = _rank1_w2(E, H, I, dtype, rng)
+    if Is:
+        c = 1 + rng.integers(0, 8, Is) / 8
+        d["sw2"] = _bits_of(a[:, None] * c[None, :], dtype)
+    cfg = OracleCfg(hidden=H, n_experts=E, top_k=k, inter=I, shared_inter=Is, dtype=dtype,
+                    has_shared_gate=gate)
+    r = oracle.moe_forward(cfg, d["x"], d["wr"], d["w13"], d["w2"], d["sw13"], d["sw2"], d["swg"])
+    ratio = r["out"] / a[None, :]
+    assert np.all(np.abs(ratio[:, 0]) > 1e-6)
+    np.testing.assert_allclose(ratio, np.repeat(ratio[:, :1], H, axis=1), rtol=1e-12, atol=0)
+
+
 # ----------------------------------------------------------- closed forms
 def _closed_form_case(H, E, k, I, Is, c, cs, dtype, gate, rng, T=2):
     """x = 1; gate rows = c/H, up rows = 1/H; W2 = 1 -> every routed expert
