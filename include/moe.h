@@ -161,7 +161,10 @@ MOE_API moe_status_t moe_router_topk(const moe_cfg_t* cfg, const void* x, const 
  * shared_w13 / shared_w2 must be NULL iff cfg->shared_inter == 0;
  * shared_gate_w must be NULL iff cfg->has_shared_gate == 0.
  * The launch uses one CTA per SM (at most) whose CTAs exchange the router
- * logits and the activations through the workspace with bounded waits; it is
+ * logits and the activations through the workspace with bounded waits, so all
+ * of them must be resident at once: a launch the occupancy calculator says
+ * the device cannot hold is refused with MOE_ERR_UNSUPPORTED (a device whose
+ * SMs are partly taken by other work is only caught by the wait limit); it is
  * enqueued with programmatic dependent launch so a following call on the same
  * stream can start its prologue early.  `out` must not alias any input. */
 MOE_API moe_status_t moe_decode_forward(const moe_cfg_t* cfg, const void* x, const void* router_w,
@@ -192,23 +195,26 @@ MOE_API moe_status_t moe_grouped_forward(const moe_cfg_t* cfg, const void* x, co
  * (moe_workspace_bytes(cfg, 1)) is larger is rejected with
  * MOE_ERR_UNSUPPORTED.  The first call on each device looks up the array's
  * device address (cudaGetSymbolAddress) with that device current; make that
- * first call before any stream capture.  Each call zero-fills the part of the
- * array it uses on `stream`, then enqueues the same kernel as
- * moe_decode_forward; it allocates nothing.  All calls share the one array, so
- * calls that can overlap on the GPU (other streams, other host threads) race
- * and must be serialised by the caller.  The device status word is in that
- * array too: moe_query_status cannot read it; host-side errors are returned
- * as for every other call.  Arguments as moe_decode_forward, minus the
- * workspace. */
+ * first call before any stream capture.  Every argument is validated before
+ * anything is enqueued.  Each call then zero-fills the part of the array it
+ * uses on `stream` (all but the device status word) and enqueues the same
+ * kernel as moe_decode_forward; it allocates nothing.  All calls share the one
+ * array, so calls that can overlap on the GPU (other streams, other host
+ * threads) race and must be serialised by the caller.  The device status word
+ * is in that array and survives later calls: moe_query_status(NULL, stream)
+ * reads and clears it.  Host-side errors are returned as for every other
+ * call.  Arguments as moe_decode_forward, minus the workspace. */
 #define MOE_NOALLOC_SCRATCH_BYTES (256u * 1024u)
 MOE_API moe_status_t moe_decode_forward_noalloc(const moe_cfg_t* cfg, const void* x, const void* router_w,
                                                 const void* w13, const void* w2, const void* shared_w13,
                                                 const void* shared_w2, const void* shared_gate_w,
                                                 moe_topk_t topk, void* out, void* stream);
 
-/* Synchronise `stream`, then read and clear the device status word of `ws`.
- * Returns MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE (or MOE_ERR_CUDA if the
- * synchronisation failed); moe_last_error() then names the check that fired. */
+/* Synchronise `stream`, then read and clear the device status word of `ws`
+ * (ws == NULL: the word in the built-in array of moe_decode_forward_noalloc on
+ * the current device).  Returns MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE (or
+ * MOE_ERR_CUDA if the synchronisation failed); moe_last_error() then names the
+ * check that fired. */
 MOE_API moe_status_t moe_query_status(void* ws, void* stream);
 
 /* Text for the last error returned on this thread ("" if none). */

@@ -181,7 +181,9 @@ def moe_workspace_init(ws: torch.Tensor, stream=None):
     _check(_load().moe_workspace_init(_ptr(ws), ws.numel(), _stream(stream)))
 
 
-def moe_query_status(ws: torch.Tensor, stream=None):
+def moe_query_status(ws: torch.Tensor | None, stream=None):
+    """Synchronise the stream, then read and clear the device status word of
+    ``ws`` (None: the built-in array of moe_decode_forward_noalloc)."""
     _check(_load().moe_query_status(_ptr(ws), _stream(stream)))
 
 

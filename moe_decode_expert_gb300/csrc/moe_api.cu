@@ -56,6 +56,11 @@ int sm_count() {
 }
 
 static std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+
+std::mutex& attr_mutex() {
+  static std::mutex mu;
+  return mu;
+}
 uint64_t wait_timeout_ns() { return g_timeout_ns.load(std::memory_order_relaxed); }
 
 // ---------------------------------------------------------- workspace layout
@@ -149,7 +154,7 @@ static moe_status_t check_ptr(const void* p, const char* name) {
   return MOE_OK;
 }
 
-static moe_status_t check_ws(const moe_cfg_t& c, const void* ws, size_t ws_bytes, int32_t T, WsLayout& L) {
+moe_status_t check_ws(const moe_cfg_t& c, const void* ws, size_t ws_bytes, int32_t T, WsLayout& L) {
   L = ws_layout(c, T);
   if (!ws) return set_error(MOE_ERR_WORKSPACE, "workspace is NULL (%zu bytes needed)", L.total);
   if (reinterpret_cast<uintptr_t>(ws) % kWsAlign)
@@ -159,9 +164,9 @@ static moe_status_t check_ws(const moe_cfg_t& c, const void* ws, size_t ws_bytes
   return MOE_OK;
 }
 
-static moe_status_t check_block(const moe_cfg_t* c, const void* x, const void* router_w, const void* w13,
-                                const void* w2, const void* sw13, const void* sw2, const void* swg,
-                                moe_topk_t topk, const void* out) {
+moe_status_t check_block(const moe_cfg_t* c, const void* x, const void* router_w, const void* w13,
+                         const void* w2, const void* sw13, const void* sw2, const void* swg, moe_topk_t topk,
+                         const void* out) {
   if (moe_status_t s = check_cfg(c)) return s;
   if (moe_status_t s = check_ptr(x, "x")) return s;
   if (moe_status_t s = check_ptr(router_w, "router_w")) return s;
@@ -282,7 +287,10 @@ moe_status_t moe_grouped_forward(const moe_cfg_t* cfg, const void* x, const void
 }
 
 moe_status_t moe_query_status(void* ws, void* stream) {
-  if (!ws) return set_error(MOE_ERR_WORKSPACE, "workspace is NULL");
+  if (!ws) {
+    // The allocation-free entry keeps its status word in its built-in array.
+    if (moe_status_t s = noalloc_scratch(&ws)) return s;
+  }
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(st) != cudaSuccess) return check_launch("cudaStreamSynchronize");
   uint32_t hdr[2] = {0, 0};

@@ -846,19 +846,47 @@ size_t decode_smem_bytes(const moe_cfg_t& c, int G) {
   return t;
 }
 
-template <int DT, int DEPTH, int MODE>
-static moe_status_t launch_decode_dt(const DecodeArgs& args, int G, size_t smem, cudaStream_t st) {
-  static int configured_dev = -1;
-  static size_t configured_smem = 0;
+// CTAs of `kernel` (kDecThreads threads, `smem` bytes of dynamic shared
+// memory) that can be resident on one SM, from the occupancy calculator;
+// cached per (device, kernel, smem) under the attribute lock.
+template <typename K>
+static int resident_ctas_per_sm(K kernel, size_t smem) {
+  struct Entry {
+    int dev;
+    const void* fn;
+    size_t smem;
+    int n;
+  };
+  static Entry cache[32];
+  static int used = 0;
   int dev = 0;
   cudaGetDevice(&dev);
-  if (configured_dev != dev || configured_smem < smem) {
-    if (cudaFuncSetAttribute(decode_fused_kernel<DT, DEPTH, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return check_launch("cudaFuncSetAttribute(decode)");
-    configured_dev = dev;
-    configured_smem = smem;
+  std::lock_guard<std::mutex> lock(attr_mutex());
+  for (int i = 0; i < used; ++i)
+    if (cache[i].dev == dev && cache[i].fn == reinterpret_cast<const void*>(kernel) && cache[i].smem == smem)
+      return cache[i].n;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kDecThreads, smem) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
   }
+  if (used < 32) cache[used++] = Entry{dev, reinterpret_cast<const void*>(kernel), smem, n};
+  return n;
+}
+
+template <int DT, int DEPTH, int MODE>
+static moe_status_t launch_decode_dt(const DecodeArgs& args, int G, size_t smem, cudaStream_t st) {
+  auto kernel = decode_fused_kernel<DT, DEPTH, MODE>;
+  if (raise_smem_limit(kernel, smem) != cudaSuccess) return check_launch("cudaFuncSetAttribute(decode)");
+  // The CTAs exchange logits and activations through memory and wait for one
+  // another, so all G of them must be resident at once: refuse a launch the
+  // device cannot hold instead of letting its waits run into the time limit.
+  const int per_sm = resident_ctas_per_sm(kernel, smem);
+  if (per_sm < 0) return set_error(MOE_ERR_CUDA, "decode: occupancy query failed");
+  if (static_cast<long long>(per_sm) * sm_count() < G)
+    return set_error(MOE_ERR_UNSUPPORTED,
+                     "decode: %d CTAs must be co-resident but only %d per SM x %d SMs fit "
+                     "(%zu B of shared memory per CTA)", G, per_sm, sm_count(), smem);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(G);
   cfg.blockDim = dim3(kDecThreads);
@@ -869,8 +897,7 @@ static moe_status_t launch_decode_dt(const DecodeArgs& args, int G, size_t smem,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, decode_fused_kernel<DT, DEPTH, MODE>, args) != cudaSuccess)
-    return check_launch("decode_fused_kernel");
+  if (cudaLaunchKernelEx(&cfg, kernel, args) != cudaSuccess) return check_launch("decode_fused_kernel");
   stat_kernels(1);
   return MOE_OK;
 }

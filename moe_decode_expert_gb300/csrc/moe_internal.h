@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "moe.h"
 
 namespace moe {
@@ -50,6 +52,17 @@ struct WsLayout {
 };
 
 WsLayout ws_layout(const moe_cfg_t& c, int32_t T);
+
+// Host-side validation of one block call's arguments (cfg, pointers,
+// aliasing) and of a workspace for T tokens (fills L).  No CUDA call.
+moe_status_t check_block(const moe_cfg_t* c, const void* x, const void* router_w, const void* w13,
+                         const void* w2, const void* sw13, const void* sw2, const void* swg, moe_topk_t topk,
+                         const void* out);
+moe_status_t check_ws(const moe_cfg_t& c, const void* ws, size_t ws_bytes, int32_t T, WsLayout& L);
+
+// Device address of the allocation-free entry's built-in scratch array on the
+// current device (looked up once per device), for moe_query_status(NULL).
+moe_status_t noalloc_scratch(void** out);
 
 // Host-side error recording (thread-local text + code).
 moe_status_t set_error(moe_status_t code, const char* fmt, ...);
@@ -108,11 +121,16 @@ moe_status_t launch_tc_router(const moe_cfg_t& c, const void* x, const void* rou
 moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws, const WsLayout& L, int32_t T,
                               int fused_nsplit, cudaStream_t st);
 
+// Serialises every read-then-raise of a kernel attribute (any host thread).
+std::mutex& attr_mutex();
+
 // Raise, never lower, a kernel's dynamic shared-memory limit on the current
 // device: a graph captured with a larger launch still runs after a call that
-// needed less.
+// needed less.  The check and the set run under one process-wide lock, so two
+// host threads cannot interleave them and lower a limit the other just set.
 template <typename K>
 inline cudaError_t raise_smem_limit(K kernel, size_t bytes) {
+  std::lock_guard<std::mutex> lock(attr_mutex());
   cudaFuncAttributes fa;
   cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
   if (e != cudaSuccess) return e;

@@ -15,7 +15,9 @@
 // two calls that can overlap on the GPU (different streams, or the same
 // array used from two threads) race and must be serialised by the caller.
 // Each call clears the part of the array it uses before its kernel runs, so
-// no state carries over from the previous call.
+// no state carries over from the previous call, except the device status
+// word: a device-side error (a wait that ran out) stays recorded until
+// moe_query_status(NULL, stream) reads and clears it.
 
 #include <mutex>
 
@@ -32,7 +34,7 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes]
 static std::mutex g_noalloc_mu;
 static void* g_noalloc_addr[64];
 
-static moe_status_t noalloc_scratch(void** out) {
+moe_status_t noalloc_scratch(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return check_launch("cudaGetDevice");
   if (dev < 0 || dev >= 64) return set_error(MOE_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
@@ -64,11 +66,19 @@ extern "C" moe_status_t moe_decode_forward_noalloc(const moe_cfg_t* cfg, const v
                      "moe_decode_forward_noalloc: this cfg needs %zu bytes of scratch, the built-in "
                      "array holds %zu (use moe_decode_forward with a workspace)",
                      need, kNoAllocScratchBytes);
+  // Every argument is checked before anything is enqueued, so a rejected call
+  // leaves the shared array (and any call still running on it) untouched.
+  if (moe_status_t s = check_block(cfg, x, router_w, w13, w2, shared_w13, shared_w2, shared_gate_w, topk, out))
+    return s;
   void* scratch = nullptr;
   if (moe_status_t s = noalloc_scratch(&scratch)) return s;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // Start every call from a zeroed control block and zeroed exchange words.
-  if (cudaMemsetAsync(scratch, 0, need, st) != cudaSuccess) return check_launch("cudaMemsetAsync(scratch)");
+  // Start every call from a zeroed control block and zeroed exchange words,
+  // except the first two words (device status, detail): an error recorded by
+  // an earlier call stays there until moe_query_status(NULL, ...) reads it.
+  constexpr size_t kKeep = 2 * sizeof(uint32_t);
+  if (cudaMemsetAsync(static_cast<uint8_t*>(scratch) + kKeep, 0, need - kKeep, st) != cudaSuccess)
+    return check_launch("cudaMemsetAsync(scratch)");
   return moe_decode_forward(cfg, x, router_w, w13, w2, shared_w13, shared_w2, shared_gate_w, topk, out,
                             scratch, need, stream);
 }

@@ -1,12 +1,14 @@
 """GPU parity of moe_grouped_forward (T > 1: device-side grouping per expert)
-against the oracle; tokens are independent, so sampled tokens of large T are
-checked one by one and token permutation is checked at full size."""
+against the oracle.  Every token is checked up to T = 512 (small-batch
+workload at T = 2..64, chunked prefill at T = 512 on both paths); at T = 4096
+a seeded 512-token subset is (tokens are independent rows).  Token
+permutation is checked at full size."""
 import numpy as np
 import pytest
 import torch
 
 import moe_synth
-from tests._util import oracle_full, oracle_sampled, parity, min_rank_gap
+from tests._util import check_tokens, oracle_full, oracle_sampled, oracle_tokens, parity, min_rank_gap
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -33,6 +35,18 @@ def _grouped(m, wl, g, T, out_dtype=None, ws=None, flags=0):
     return ids, w, out
 
 
+_REF = {}
+
+
+def _ref_tokens(wl, layer, T, g, tokens):
+    """Oracle rows for (workload, layer, T, tokens), computed once per module
+    (both paths of a parametrised test see the same seeded inputs)."""
+    key = (wl.name, layer, T, tuple(tokens))
+    if key not in _REF:
+        _REF[key] = oracle_tokens(wl, g, tokens)
+    return _REF[key]
+
+
 def _check_tokens(ids, w, out, ref, tokens, k):
     ok = 0
     for i, t in enumerate(tokens):
@@ -56,9 +70,8 @@ def test_small_batch_zipf(m, T, flags):
     ids, w, out = _grouped(m, wl, g, T, flags=flags)
     st = m.moe_get_stats()
     assert st["grouped_calls"] == 1 and st["grouped_tc_calls"] == (1 if flags == TC else 0)
-    tokens = list(range(T)) if T <= 8 else sorted(np.random.default_rng(T).choice(T, 8, replace=False).tolist())
-    ref = oracle_sampled(wl, g, tokens)
-    _check_tokens(ids, w, out, ref, tokens, wl.top_k)
+    tokens = list(range(T))  # every token
+    check_tokens(ids, w, out, _ref_tokens(wl, 0, T, g, tokens), tokens, wl.top_k)
 
 
 @pytest.mark.parametrize("T", [9, 16, 17, 31, 32, 33])
@@ -78,10 +91,8 @@ def test_small_batch_fused_ranking_boundary(m, T):
     # W13, W2, combine
     expect = (1 + 1 if T <= 32 else 2 + 2) + (0 if T <= 16 else 1) + 3
     assert st["kernels_launched"] == expect
-    picks = np.random.default_rng(T).choice(T, 6, replace=False).tolist()
-    tokens = sorted(set([0, T - 1] + picks))
-    ref = oracle_sampled(wl, g, tokens)
-    _check_tokens(ids, w, out, ref, tokens, wl.top_k)
+    tokens = list(range(T))  # every token
+    check_tokens(ids, w, out, _ref_tokens(wl, 2, T, g, tokens), tokens, wl.top_k)
 
 
 @pytest.mark.parametrize("flags", [SIMT, TC], ids=["simt", "tcgen05"])
@@ -136,9 +147,8 @@ def test_chunked_prefill_512(m, flags):
     T = 512
     g = moe_synth.make_layer(wl, 0, T, device=DEV)
     ids, w, out = _grouped(m, wl, g, T, flags=flags)
-    tokens = [0, 1, 255, 256, 511] + sorted(np.random.default_rng(5).choice(T, 3, replace=False).tolist())
-    ref = oracle_sampled(wl, g, tokens)
-    _check_tokens(ids, w, out, ref, tokens, wl.top_k)
+    tokens = list(range(T))  # every token, at the full-width tile shapes
+    check_tokens(ids, w, out, _ref_tokens(wl, 0, T, g, tokens), tokens, wl.top_k)
 
 
 def test_chunked_prefill_4096_tcgen05(m):
@@ -146,9 +156,11 @@ def test_chunked_prefill_4096_tcgen05(m):
     T = 4096
     g = moe_synth.make_layer(wl, 0, T, device=DEV)
     ids, w, out = _grouped(m, wl, g, T, flags=TC)
-    tokens = [0, 4095] + sorted(np.random.default_rng(9).choice(T, 4, replace=False).tolist())
-    ref = oracle_sampled(wl, g, tokens)
-    _check_tokens(ids, w, out, ref, tokens, wl.top_k)
+    # a seeded 512-token subset, plus the first and last token
+    pick = np.random.default_rng(9).choice(np.arange(1, T - 1), 510, replace=False).tolist()
+    tokens = sorted(set([0, T - 1] + pick))
+    assert len(tokens) == 512
+    check_tokens(ids, w, out, _ref_tokens(wl, 0, T, g, tokens), tokens, wl.top_k)
 
 
 def test_simt_and_tcgen05_paths_agree(m):

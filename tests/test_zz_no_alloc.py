@@ -5,7 +5,9 @@ start-up, a plugin host that only hands over tensor pointers), so they cannot
 provide the workspace moe_decode_forward needs.  moe_decode_forward_noalloc
 keeps that scratch in a fixed array inside the library instead.  This test
 calls it twice in a row and compares each result with moe_decode_forward on
-the same inputs, within the tolerance the other parity tests use."""
+the same inputs, within the tolerance the other parity tests use, and with the
+oracle.  Its device status word lives in the same array; a wait that runs out
+stays recorded there until moe_query_status(NULL) reads it."""
 import ctypes
 
 import numpy as np
@@ -13,7 +15,7 @@ import pytest
 import torch
 
 import moe_synth
-from tests._util import parity
+from tests._util import _check_one_token, oracle_sampled, parity
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -59,6 +61,44 @@ def test_noalloc_matches_workspace_entry_two_calls(m, name):
         assert torch.equal(ids0, ids1)
         np.testing.assert_allclose(w1.cpu().numpy(), w0.cpu().numpy(), rtol=1e-6)
         parity(out1, out0.double().cpu().numpy())
+        _check_one_token(ids1, w1, out1, oracle_sampled(wl, g, [0]), wl.top_k)
+    m.moe_query_status(None)  # no device-side error recorded in the built-in array
+
+
+def test_noalloc_device_timeout_is_reported_and_later_calls_recover(m):
+    """With a 1 us limit on every device wait, a full-width call almost surely
+    has a CTA whose wait for the others runs out; the kernel records that in
+    the array's status word and returns (no trap).  A later call with the
+    normal limit computes the right result, leaves the recorded error in
+    place, and moe_query_status(NULL) then reports and clears it."""
+    wl = moe_synth.workload("full_decode")
+    cfg = m.cfg_from_workload(wl)
+    g = moe_synth.make_layer(wl, 3, 1, device=DEV)
+    ref = oracle_sampled(wl, g, [0])
+    ids = torch.empty(1, wl.top_k, dtype=torch.int32, device=DEV)
+    w = torch.empty(1, wl.top_k, dtype=torch.float32, device=DEV)
+    out = torch.empty(1, wl.hidden, dtype=cfg.out_torch_dtype, device=DEV)
+    m.moe_query_status(None)
+    seen = False
+    for _ in range(20):
+        try:
+            m.moe_set_wait_timeout_ns(1000)
+            _noalloc(m, cfg, g, ids, w, out)
+        finally:
+            m.moe_set_wait_timeout_ns(2_000_000_000)
+        ids.fill_(-1)
+        out.fill_(float("nan"))
+        _noalloc(m, cfg, g, ids, w, out)  # normal limit: must be right
+        torch.cuda.synchronize()
+        _check_one_token(ids, w, out, ref, wl.top_k)
+        try:
+            m.moe_query_status(None)
+        except m.MoeError as e:
+            assert e.code == 5, e  # MOE_ERR_TIMEOUT, recorded by the 1 us call
+            seen = True
+            break
+    assert seen, "no wait ran out in 20 calls with a 1 us limit"
+    m.moe_query_status(None)  # read once, then clear
 
 
 def test_noalloc_rejects_configs_beyond_its_scratch(m):
