@@ -96,7 +96,7 @@ typedef struct moe_cfg {
   int32_t norm_topk;       /* 1: renormalise the k weights to sum 1; 0: keep
                               the full-softmax probabilities                    */
   int32_t has_shared_gate; /* 1: shared output scaled by sigmoid(x . wg)       */
-  int32_t flags;           /* 0, or one MOE_FLAG_GROUPED_* bit (T > 1 path)    */
+  int32_t flags;           /* MOE_FLAG_* bits below (0 = defaults)             */
 } moe_cfg_t;
 
 /* cfg->flags bits selecting the T > 1 path.  With neither bit the library
@@ -112,6 +112,12 @@ typedef struct moe_cfg {
                                     routing-independent weights (router rows,
                                     shared expert) before it waits for the
                                     preceding kernel; x is always read after. */
+#define MOE_FLAG_RESIDUAL 8      /* out = x + block(x): the residual add of the
+                                    decoder layer fused into the output write
+                                    (x exact in fp32, added after the block's
+                                    sum, one rounding to out_dtype), so a stack
+                                    of layers chains out -> x with no extra
+                                    kernel.  Both the T = 1 and T > 1 paths. */
 
 /* Caller-owned routing outputs, [T, k] each (device memory). */
 typedef struct moe_topk {

@@ -58,6 +58,7 @@ class moe_stats_t(ctypes.Structure):
 MOE_FLAG_GROUPED_SIMT = 1
 MOE_FLAG_GROUPED_TC = 2
 MOE_FLAG_STATIC_WEIGHTS = 4
+MOE_FLAG_RESIDUAL = 8
 
 
 @dataclass(frozen=True)
@@ -88,6 +89,15 @@ class MoeCfg:
 
 
 _lib = None
+
+
+def use_library(path: str):
+    """Load another build of this library (the phase-trace variant) instead of
+    ``libmoe_gb300.so``; must come before the first call."""
+    global LIB_PATH
+    if _lib is not None:
+        raise RuntimeError("the library is already loaded")
+    LIB_PATH = path
 
 
 def _load():

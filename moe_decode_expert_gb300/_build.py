@@ -18,6 +18,10 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build", "moe")
 LIB = os.path.join(PKG, "libmoe_gb300.so")
+# Phase-trace variant of the library (decode kernel with global-timer stamps,
+# see trace_phases.py); never loaded by the package unless asked for.
+TRACE_BUILD = os.path.join(ROOT, "_build", "moe_trace")
+TRACE_LIB = os.path.join(PKG, "libmoe_gb300_trace.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
@@ -40,8 +44,8 @@ def _newest_dep() -> float:
     return max(os.path.getmtime(d) for d in deps)
 
 
-def _compile(src: str, extra: list[str]) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+def _compile(src: str, extra: list[str], build_dir: str = BUILD) -> str:
+    obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
     if os.path.exists(obj) and os.path.getmtime(obj) >= max(os.path.getmtime(src), _newest_dep()):
         return obj
     cmd = [_nvcc(), *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj + ".tmp"]
@@ -52,25 +56,28 @@ def _compile(src: str, extra: list[str]) -> str:
     return obj
 
 
-def build(verbose: bool = False, extra: list[str] | None = None) -> str:
-    """Compile every CUDA source and link the shared library; returns its path."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, extra: list[str] | None = None, trace: bool = False) -> str:
+    """Compile every CUDA source and link the shared library; returns its path.
+    ``trace=True`` builds the phase-trace variant (``-DMOE_PHASE_TRACE``) into
+    its own directory and library instead."""
+    build_dir, lib = (TRACE_BUILD, TRACE_LIB) if trace else (BUILD, LIB)
+    os.makedirs(build_dir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
-    extra = list(extra or [])
+    extra = list(extra or []) + (["-DMOE_PHASE_TRACE"] if trace else [])
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra), srcs))
+        objs = list(ex.map(lambda s: _compile(s, extra, build_dir), srcs))
     newest = max(os.path.getmtime(o) for o in objs)
-    if not os.path.exists(LIB) or os.path.getmtime(LIB) < newest:
-        tmp = LIB + f".tmp{os.getpid()}"
+    if not os.path.exists(lib) or os.path.getmtime(lib) < newest:
+        tmp = lib + f".tmp{os.getpid()}"
         cmd = [_nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "shared",
                "-Xlinker", "-rpath," + _cuda_lib_dir()]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
+        os.replace(tmp, lib)
     if verbose:
-        print(LIB)
-    return LIB
+        print(lib)
+    return lib
 
 
 def ptxas_report() -> str:

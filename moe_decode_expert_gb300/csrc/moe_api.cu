@@ -136,7 +136,7 @@ static moe_status_t check_cfg(const moe_cfg_t* c) {
     return set_error(MOE_ERR_INVALID_ARG, "cfg: has_shared_gate is 0 or 1");
   if (c->has_shared_gate && c->shared_inter == 0)
     return set_error(MOE_ERR_INVALID_ARG, "cfg: a shared gate needs a shared expert");
-  if (c->flags & ~(MOE_FLAG_GROUPED_SIMT | MOE_FLAG_GROUPED_TC | MOE_FLAG_STATIC_WEIGHTS))
+  if (c->flags & ~(MOE_FLAG_GROUPED_SIMT | MOE_FLAG_GROUPED_TC | MOE_FLAG_STATIC_WEIGHTS | MOE_FLAG_RESIDUAL))
     return set_error(MOE_ERR_INVALID_ARG, "cfg: unknown flag bits");
   if ((c->flags & MOE_FLAG_GROUPED_SIMT) && (c->flags & MOE_FLAG_GROUPED_TC))
     return set_error(MOE_ERR_INVALID_ARG, "cfg: MOE_FLAG_GROUPED_SIMT and MOE_FLAG_GROUPED_TC exclude each other");

@@ -35,6 +35,7 @@
 // at entry so the next call on the stream launches early and waits in its own
 // prologue.
 
+#include <atomic>
 #include <type_traits>
 
 #include "moe_common.cuh"
@@ -45,6 +46,24 @@ namespace moe {
 constexpr int kDecThreads = 256;
 constexpr int kDecWarps = kDecThreads / 32;
 constexpr int kChunks = 8;  // 16-byte chunks per lane per row kept in flight
+
+// Phase trace (built only with -DMOE_PHASE_TRACE, into a separate library):
+// thread 0 of each CTA stores the GPU global time at fixed points of the
+// kernel into a ring of per-launch records, read back by moe_trace_read.
+#ifdef MOE_PHASE_TRACE
+constexpr int kTraceSlots = 16, kTraceCtas = 256, kTraceLaunches = 64;
+__device__ uint64_t g_moe_trace[kTraceLaunches * kTraceCtas * kTraceSlots];
+static std::atomic<unsigned> g_trace_next{0};  // ring position of the next launch
+#define MOE_STAMP(s)                                                          \
+  do {                                                                        \
+    if (threadIdx.x == 0 && blockIdx.x < kTraceCtas)                          \
+      a.trace[blockIdx.x * kTraceSlots + (s)] = global_ns();                  \
+  } while (0)
+#else
+#define MOE_STAMP(s) \
+  do {               \
+  } while (0)
+#endif
 
 struct DecodeArgs {
   const uint8_t* x;
@@ -62,11 +81,15 @@ struct DecodeArgs {
   uint64_t* ll_act;
   int H, E, k, I, Is, has_gate, norm_topk, out_dtype;
   int static_weights;  // MOE_FLAG_STATIC_WEIGHTS: weight reads may precede the PDL wait
+  int residual;        // MOE_FLAG_RESIDUAL: out = x + block(x)
   int ll_stride;   // words between the copies of the logit words
   int act_stride;  // words between the copies of the activation words
   uint32_t rs_r, rs_s;  // shared-memory row strides (bytes) of the routed and shared W2 rows
   uint32_t off_xh, off_lg, off_act, off_terms, off_w2;
   uint64_t timeout_ns;
+#ifdef MOE_PHASE_TRACE
+  uint64_t* trace;  // this launch's record: [CTA][kTraceSlots]
+#endif
 };
 
 // 16-byte streaming load of a weight chunk, or zeros without a load when
@@ -337,6 +360,7 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
     }
   };
 
+  MOE_STAMP(0);  // entry
   if (tid == 0) {
     s_fail = 0;
     s_next = 0;
@@ -386,6 +410,7 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
     if (DEPTH == 1 && Is > 0) copy_w2_cols(true);
   }
   pdl_wait();  // x (and anything else an earlier kernel wrote) is visible from here
+  MOE_STAMP(1);  // PDL wait released
   if (!a.static_weights) gv.issue(ra, va, rb, vb, c0w, cb1, t);
 
   uint32_t gen_prev = 0;
@@ -408,6 +433,7 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
   if (DEPTH == 1 && !a.static_weights && Is > 0) copy_w2_cols(true);
   __syncthreads();
   const uint32_t epoch = s_epoch;
+  MOE_STAMP(2);  // x staged
 
   for (int rg = 0; rg < R1; rg += 16) {
     float acc[2][4] = {};
@@ -422,6 +448,7 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
     gemv_store_partials(s_red, warp, lane, rg, acc);
   }
   __syncthreads();
+  MOE_STAMP(3);  // phase-1 dot products summed
   // Every CTA reads all logits and every activation, so each word is
   // published in several copies (readers spread over more L2 lines):
   // eight threads per result, one copy each.
@@ -442,6 +469,7 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
                                 (cta + (nL + pi) * G - E1);
     if (rep < (logit ? kLogitReplicas : kActReplicas)) ll_store(dst, v, epoch);
   }
+  MOE_STAMP(4);  // phase-1 results published
 
   // ---- phase 2: the logits, their top-k (fp32, lower index first on ties)
   // and the routing weights.  Every logit gets a unique 64-bit key (logit
@@ -454,6 +482,7 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
       const uint64_t* src = a.ll_logits + static_cast<size_t>(cta % kLogitReplicas) * a.ll_stride;
       const bool ok = ll_gather<8>(src, lg, E + a.has_gate, lane, 32, epoch, global_ns() + a.timeout_ns);
       if (!__all_sync(0xffffffffu, ok) && lane == 0) s_fail = kDevTimeoutLogits;
+      MOE_STAMP(5);  // logits gathered
     }
     __syncthreads();
     const int i0 = warp * 32 + lane;
@@ -500,6 +529,7 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
   }
   __syncthreads();
   const bool ranked = s_fail == 0;  // uniform: read after the barrier
+  MOE_STAMP(6);  // ranked
   // warp 0: routing weights and the shared gate (then s_wready)
   auto weights = [&]() {
     if (ranked) {
@@ -515,6 +545,7 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
       __threadfence_block();
       s_wready = 1;
     }
+    MOE_STAMP(7);  // routing weights ready
   };
   if (DEPTH == 2 && warp == 0) weights();
 
@@ -641,6 +672,7 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
   // warp's gather is one round trip (the epoch tags still catch a late one).
   // A CTA counts itself in as soon as its activations are out; its own W2
   // copies land while it waits.
+  MOE_STAMP(8);  // thread 0's phase-3 work done
   __syncthreads();
   if (tid == 0 && !s_fail) {
     uint32_t* cnt = &a.ctrl->arrive[epoch & 1u];
@@ -651,9 +683,11 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
       if (global_ns() > deadline) { arrived = false; break; }
     }
     if (!arrived) s_fail = kDevTimeoutAct;
+    MOE_STAMP(9);  // every CTA counted in
   }
   cp_async_wait_all();  // this thread's W2 copies
   __syncthreads();
+  MOE_STAMP(10);  // W2 copies landed
   {
     const int g = lane >> 2, t = lane & 3;
     const int c0 = ks0 * 16, c1 = min(ks1 * 16, K);
@@ -670,6 +704,7 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
       ok = __all_sync(0xffffffffu, got);
       if (!ok && lane == 0) s_fail = kDevTimeoutAct;
     }
+    MOE_STAMP(11);  // activations gathered
     __syncwarp();
     float unsc = 1.0f;
     if (ok && ks1 > ks0) {
@@ -702,6 +737,7 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
       }
     }
     __syncwarp();  // terms and this warp's W2 copies visible to all its lanes
+    MOE_STAMP(12);  // terms written
     const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8;
     const uint32_t ta0 = smem_u32(terms) + static_cast<uint32_t>(g * Kp + 4 * t) * 2;
     const bool bl = lane < 12;  // lanes holding B columns 0-2
@@ -783,6 +819,7 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
         s_red[warp][m * 16 + g + 8] = bot * unsc;
       }
     }
+    MOE_STAMP(13);  // combine steps done
   }
   __syncthreads();
   if (!s_fail) {
@@ -790,8 +827,10 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
       float sum = 0.0f;
 #pragma unroll
       for (int w = 0; w < kDecWarps; ++w) sum += s_red[w][tid];
+      if (a.residual) sum += xs[h0 + tid];  // x, exact in fp32
       store_out(a.out, h0 + tid, sum, a.out_dtype);
     }
+    MOE_STAMP(14);  // output written
     // Every CTA has read the epoch before publishing its activations and CTA 0
     // has now seen all of them, so the next launch may use the next epoch.
     if (cta == 0 && tid == 0) atomicExch(&a.ctrl->gen, epoch);
@@ -922,6 +961,7 @@ moe_status_t launch_decode_fused(const moe_cfg_t& c, const BlockPtrs& p, uint8_t
   a.H = c.hidden; a.E = c.n_experts; a.k = c.top_k; a.I = c.inter; a.Is = c.shared_inter;
   a.has_gate = c.has_shared_gate; a.norm_topk = c.norm_topk; a.out_dtype = c.out_dtype;
   a.static_weights = (c.flags & MOE_FLAG_STATIC_WEIGHTS) ? 1 : 0;
+  a.residual = (c.flags & MOE_FLAG_RESIDUAL) ? 1 : 0;
   a.ll_stride = (c.n_experts + 2) & ~1;
   a.act_stride = (c.top_k * c.inter + c.shared_inter + 1) & ~1;
   a.rs_r = w2_row_stride(c.inter);
@@ -929,6 +969,15 @@ moe_status_t launch_decode_fused(const moe_cfg_t& c, const BlockPtrs& p, uint8_t
   size_t smem;
   decode_smem_layout(c, G, a.off_xh, a.off_lg, a.off_act, a.off_terms, a.off_w2, smem);
   a.timeout_ns = wait_timeout_ns();
+#ifdef MOE_PHASE_TRACE
+  {
+    void* base = nullptr;
+    if (cudaGetSymbolAddress(&base, g_moe_trace) != cudaSuccess) return check_launch("trace buffer");
+    a.trace = static_cast<uint64_t*>(base) +
+              static_cast<size_t>(g_trace_next++ % kTraceLaunches) * kTraceCtas * kTraceSlots;
+    if (G > kTraceCtas) return set_error(MOE_ERR_UNSUPPORTED, "trace build: more than %d CTAs", kTraceCtas);
+  }
+#endif
   if (smem > 227 * 1024)
     return set_error(MOE_ERR_UNSUPPORTED, "decode: needs %zu B of shared memory per CTA (max 232448)", smem);
   if (2 * ((c.n_experts + c.has_shared_gate + c.shared_inter + G - 1) / G) > 64)
@@ -960,3 +1009,24 @@ moe_status_t launch_decode_fused(const moe_cfg_t& c, const BlockPtrs& p, uint8_t
 }
 
 }  // namespace moe
+
+#ifdef MOE_PHASE_TRACE
+// Host side of the phase trace, exported only by the trace build: geometry,
+// reset (next launch records into ring entry 0; records zeroed) and read-back.
+extern "C" __attribute__((visibility("default"))) int moe_trace_reset(void) {
+  moe::g_trace_next = 0;
+  void* base = nullptr;
+  if (cudaGetSymbolAddress(&base, moe::g_moe_trace) != cudaSuccess) return 1;
+  return cudaMemset(base, 0, sizeof(moe::g_moe_trace)) == cudaSuccess ? 0 : 1;
+}
+extern "C" __attribute__((visibility("default"))) int moe_trace_geometry(int* slots, int* ctas, int* launches) {
+  *slots = moe::kTraceSlots;
+  *ctas = moe::kTraceCtas;
+  *launches = moe::kTraceLaunches;
+  return 0;
+}
+extern "C" __attribute__((visibility("default"))) int moe_trace_read(uint64_t* dst, size_t words) {
+  if (words > sizeof(moe::g_moe_trace) / 8) return 1;
+  return cudaMemcpyFromSymbol(dst, moe::g_moe_trace, words * 8) == cudaSuccess ? 0 : 1;
+}
+#endif

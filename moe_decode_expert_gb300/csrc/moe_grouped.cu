@@ -182,7 +182,8 @@ __global__ void __launch_bounds__(kGThreads) grouped_w2_kernel(
 
 // ---------------------------------------------------------------- combine
 __global__ void __launch_bounds__(256) combine_kernel(const float* y, int T, int H, int k,
-                                                      int has_shared, void* out, int out_dtype) {
+                                                      int has_shared, void* out, int out_dtype,
+                                                      const uint16_t* xres, int x_dtype) {
   pdl_launch_dependents();  // let the next kernel on the stream launch early
   pdl_wait();               // inputs written by the previous kernel are visible
   // grid (ceil(H/4 / 256), T): four consecutive outputs of token blockIdx.y per
@@ -209,6 +210,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* y, int T, int
       if (j0 + u < nk) { acc.x += v[u].x; acc.y += v[u].y; acc.z += v[u].z; acc.w += v[u].w; }
   }
   const size_t o = static_cast<size_t>(t) * H + 4 * h4;
+  if (xres) {  // residual add (MOE_FLAG_RESIDUAL): out = x + block(x)
+    const uint2 r = *reinterpret_cast<const uint2*>(xres + o);
+    const float2 a = x_dtype == MOE_BF16 ? unpack2<MOE_BF16>(r.x) : unpack2<MOE_F16>(r.x);
+    const float2 b = x_dtype == MOE_BF16 ? unpack2<MOE_BF16>(r.y) : unpack2<MOE_F16>(r.y);
+    acc.x += a.x; acc.y += a.y; acc.z += b.x; acc.w += b.y;
+  }
   store_out(out, o, acc.x, out_dtype);
   store_out(out, o + 1, acc.y, out_dtype);
   store_out(out, o + 2, acc.z, out_dtype);
@@ -288,7 +295,9 @@ moe_status_t launch_grouped(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws,
     if (moe_status_t s = check_launch("grouped_w2_kernel")) return s;
     stat_kernels(2);
   }
-  launch_pdl(combine_kernel, dim3((H / 4 + 255) / 256, T), dim3(256), 0, st, y, T, H, k, Is > 0, p.out, c.out_dtype);
+  const uint16_t* xres = (c.flags & MOE_FLAG_RESIDUAL) ? static_cast<const uint16_t*>(p.x) : nullptr;
+  launch_pdl(combine_kernel, dim3((H / 4 + 255) / 256, T), dim3(256), 0, st, y, T, H, k, Is > 0, p.out,
+             c.out_dtype, xres, c.dtype);
   if (moe_status_t s = check_launch("combine_kernel")) return s;
   stat_kernels(1);
   return MOE_OK;

@@ -60,7 +60,7 @@ def _topk(m):
 
 @pytest.mark.parametrize("field,value,code", [
     ("hidden", 0, 1), ("inter", 12, 2), ("top_k", 33, 2), ("top_k", 0, 1), ("dtype", 3, 2),
-    ("n_experts", 2000, 2), ("flags", 8, 1), ("flags", 3, 1), ("norm_topk", 2, 1),
+    ("n_experts", 2000, 2), ("flags", 16, 1), ("flags", 3, 1), ("norm_topk", 2, 1),
 ])
 def test_bad_cfg_is_rejected_on_host(m, field, value, code):
     c = m.MoeCfg(256, 16, 2, 64, 0, m.MOE_F16).c()

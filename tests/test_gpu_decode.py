@@ -325,3 +325,83 @@ def test_chained_layers_read_the_previous_output(m, flags):
     m.moe_query_status(ws)
     for a, b in zip(eager, bufs[1:]):
         assert torch.equal(a, b)
+
+
+def _ulp(v, dt):
+    """Spacing of the storage type (fp16 / bf16) at |v| (normal range; the
+    subnormal spacing below it)."""
+    mant, emin = (10, -14) if dt == torch.float16 else (7, -126)
+    e = np.floor(np.log2(np.maximum(np.abs(v), 2.0 ** emin)))
+    return 2.0 ** (e - mant)
+
+
+@pytest.mark.parametrize("name,flags", [("full_decode", 8 | 4), ("sharded_decode", 8)],
+                         ids=["full_width_static", "sharded"])
+def test_residual_chain_layers(m, name, flags):
+    """h <- h + MoE_l(h) over 4 layers, the residual add fused into the output
+    write (MOE_FLAG_RESIDUAL): each layer reads the previous layer's output.
+    Every layer is checked against x_l + oracle(x_l) on the input x_l the GPU
+    actually used: within the tolerance, and elementwise within half a
+    storage-type ulp of that sum plus 1e-3 of the block's own output scale.
+    Eager and graph-replayed chains agree bit for bit."""
+    wl = moe_synth.workload(name)
+    cfg = m.cfg_from_workload(wl, None, flags)
+    L = 4
+    layers = [moe_synth.make_layer(wl, l + 5, 1, device=DEV, weights_only=True) for l in range(L)]
+    bufs = [moe_synth.make_x(wl, 5, 1, DEV)] + [torch.empty(1, wl.hidden, dtype=wl.torch_dtype, device=DEV)
+                                                for _ in range(L)]
+    ids = [torch.empty(1, wl.top_k, dtype=torch.int32, device=DEV) for _ in range(L)]
+    wts = [torch.empty(1, wl.top_k, dtype=torch.float32, device=DEV) for _ in range(L)]
+    ws = m.alloc_workspace(cfg, 1, DEV)
+
+    def step():
+        for l, g in enumerate(layers):
+            m.moe_decode_forward(cfg, bufs[l], g["router_w"], g["w13"], g["w2"], g["shared_w13"], g["shared_w2"],
+                                 g["shared_gate_w"], ids[l], wts[l], bufs[l + 1], ws)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.synchronize()
+    m.moe_query_status(ws)
+    for l, g in enumerate(layers):
+        ref = oracle_sampled(wl, {**g, "x": bufs[l]}, [0])
+        xl = bufs[l].double().cpu().numpy()
+        exact = xl + ref["out"]
+        got = bufs[l + 1].double().cpu().numpy()
+        if min_rank_gap(ref["logits"], wl.top_k)[0] > 1e-4:
+            assert np.array_equal(ids[l].cpu().numpy(), ref["ids"])
+        parity(bufs[l + 1], exact)
+        bound = 0.5 * _ulp(exact, wl.torch_dtype) + 1e-3 * np.abs(ref["out"]).max()
+        assert np.all(np.abs(got - exact) <= bound), np.abs(got - exact).max()
+    eager = [b.clone() for b in bufs[1:]]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        step()
+    for b in bufs[1:]:
+        b.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    m.moe_query_status(ws)
+    for a, b in zip(eager, bufs[1:]):
+        assert torch.equal(a, b)
+
+
+def test_residual_flag_adds_x_after_the_block(m):
+    """With fp32 output the residual result is exactly fl(block(x) + x): the
+    add comes after the block's own sum, on x decoded exactly."""
+    wl = moe_synth.workload("full_decode")
+    g = moe_synth.make_layer(wl, 7, 1, device=DEV)
+    outs = []
+    for flags in (0, 8):
+        cfg = m.cfg_from_workload(wl, 3, flags)
+        ids = torch.empty(1, wl.top_k, dtype=torch.int32, device=DEV)
+        w = torch.empty(1, wl.top_k, dtype=torch.float32, device=DEV)
+        out = torch.empty(1, wl.hidden, dtype=torch.float32, device=DEV)
+        ws = m.alloc_workspace(cfg, 1, DEV)
+        m.moe_decode_forward(cfg, g["x"], g["router_w"], g["w13"], g["w2"], g["shared_w13"], g["shared_w2"],
+                             g["shared_gate_w"], ids, w, out, ws)
+        m.moe_query_status(ws)
+        outs.append(out)
+    assert torch.equal(outs[1], outs[0] + g["x"].float())

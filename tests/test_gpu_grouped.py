@@ -206,3 +206,18 @@ def test_graph_replays_after_a_smaller_call(m):
     torch.cuda.synchronize()
     m.moe_query_status(ws)
     assert torch.equal(out, eager)
+
+
+@pytest.mark.parametrize("flags", [SIMT, TC], ids=["simt", "tcgen05"])
+def test_residual_flag_grouped(m, flags):
+    """MOE_FLAG_RESIDUAL on the T > 1 path: with fp32 output the result is
+    exactly fl(block(x) + x) per element (the add follows the slot-order sum);
+    with bf16 output it is that sum rounded once."""
+    wl = moe_synth.workload("small_batch")
+    T = 8
+    g = moe_synth.make_layer(wl, 6, T, device=DEV)
+    _, _, o0 = _grouped(m, wl, g, T, out_dtype=3, flags=flags)
+    _, _, o1 = _grouped(m, wl, g, T, out_dtype=3, flags=flags | 8)
+    assert torch.equal(o1, o0 + g["x"].float())
+    _, _, o2 = _grouped(m, wl, g, T, flags=flags | 8)
+    assert torch.equal(o2, o1.to(torch.bfloat16))
