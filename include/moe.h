@@ -216,6 +216,26 @@ MOE_API moe_status_t moe_decode_forward_noalloc(const moe_cfg_t* cfg, const void
                                                 const void* shared_w2, const void* shared_gate_w,
                                                 moe_topk_t topk, void* out, void* stream);
 
+/* Sum of per-shard partial outputs, for tensor-parallel use ("BI-V100
+ * inference work log", Part 2: TP = 4 splits each expert's intermediate size I
+ * = 512 into 128 per GPU; Part 9 and the "Decode throughput analysis report",
+ * module profiling: one all-reduce of the MoE output per layer).  Shard r of
+ * G holds W13 rows [r*I/G, (r+1)*I/G) of the gate and of the up block, W2
+ * columns [r*I/G, (r+1)*I/G), the same slices of the shared expert, and the
+ * full router and shared-gate vector; a decode or grouped call on it with
+ * cfg->inter = I/G, cfg->shared_inter = Is/G and out_dtype = MOE_F32 gives a
+ * partial output whose sum over the shards is the block's output.
+ *   partials [n_parts, n] fp32 (device), summed in part order;
+ *   residual [n] (optional, may be NULL) of residual_dtype (MOE_F16/MOE_BF16)
+ *   added after the sum (the decoder layer's residual add);
+ *   out [n] of out_dtype (MOE_F16, MOE_BF16 or MOE_F32), one rounding.
+ * n must be a multiple of 8 and every pointer 16-byte aligned.  Across GPUs,
+ * all-reduce the fp32 partials first and call this with n_parts = 1.
+ * Enqueued with programmatic dependent launch; `out` must not alias the
+ * partials. */
+MOE_API moe_status_t moe_sum_partials(const float* partials, int32_t n_parts, int64_t n, const void* residual,
+                                      int32_t residual_dtype, void* out, int32_t out_dtype, void* stream);
+
 /* Synchronise `stream`, then read and clear the device status word of `ws`
  * (ws == NULL: the word in the built-in array of moe_decode_forward_noalloc on
  * the current device).  Returns MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE (or

@@ -32,7 +32,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 EXPORTS = ("moe_abi_version", "moe_workspace_bytes", "moe_workspace_init", "moe_router_topk",
            "moe_decode_forward", "moe_grouped_forward", "moe_query_status", "moe_last_error",
            "moe_get_stats", "moe_reset_stats", "moe_set_wait_timeout_ns", "moe_test_wait_timeout",
-           "moe_decode_forward_noalloc")
+           "moe_decode_forward_noalloc", "moe_sum_partials")
 
 
 class MoeError(RuntimeError):
@@ -125,6 +125,7 @@ def _load():
         "moe_set_wait_timeout_ns": ([u64], ctypes.c_int),
         "moe_test_wait_timeout": ([vp, sz, vp], ctypes.c_int),
         "moe_decode_forward_noalloc": ([cfgp, vp, vp, vp, vp, vp, vp, vp, moe_topk_t, vp, vp], ctypes.c_int),
+        "moe_sum_partials": ([vp, i32, ctypes.c_int64, vp, i32, vp, i32, vp], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -281,6 +282,26 @@ def moe_grouped_forward(cfg: MoeCfg, x, router_w, w13, w2, shared_w13, shared_w2
     args = _block_args(cfg, x, router_w, w13, w2, shared_w13, shared_w2, shared_gate_w, ids, weights, out, T)
     c = cfg.c()
     _check(_load().moe_grouped_forward(ctypes.byref(c), *args, _ptr(ws), ws.numel(), T, _stream(stream)))
+
+
+def moe_sum_partials(partials, out, residual=None, stream=None):
+    """out = sum over dim 0 of fp32 ``partials`` [n_parts, ...] (+ residual),
+    rounded once to out's dtype; the sum runs in part order."""
+    if partials.dtype != torch.float32 or not partials.is_contiguous():
+        raise ValueError("partials must be contiguous fp32")
+    n = out.numel()
+    if partials.numel() != partials.shape[0] * n or not out.is_contiguous():
+        raise ValueError("partials must be [n_parts, *out.shape], out contiguous")
+    if out.device != partials.device:
+        raise ValueError("partials and out must be on one device")
+    rdt = 0
+    if residual is not None:
+        if residual.numel() != n or not residual.is_contiguous() or residual.dtype not in (torch.float16,
+                                                                                           torch.bfloat16):
+            raise ValueError("residual must be a contiguous fp16/bf16 tensor shaped like out")
+        rdt = _DT_CODE[residual.dtype]
+    _check(_load().moe_sum_partials(_ptr(partials), partials.shape[0], n, _ptr(residual), rdt, _ptr(out),
+                                    _DT_CODE[out.dtype], _stream(stream)))
 
 
 def cfg_from_workload(wl, out_dtype=None, flags=0) -> MoeCfg:

@@ -134,11 +134,7 @@ def make_layer(wl: Workload, layer: int = 0, T: int | None = None, device="cpu",
         d["x"] = x
     if x_only:
         return d
-    wr = _normal((E, H), wl.router_std, seed_of(wl, layer, _WR, seed_base), device, dt)
-    if wl.routing == "zipf":
-        r = torch.from_numpy(zipf_ranks(wl, layer, seed_base).astype(np.float64))
-        wr[:, 0] = (-wl.zipf_s * torch.log(r)).to(dt).to(wr.device)
-    d["router_w"] = wr
+    d["router_w"] = make_router(wl, layer, device, seed_base)
     d["w13"] = _normal((E, 2 * I, H), wl.w_std, seed_of(wl, layer, _W13, seed_base), device, dt)
     d["w2"] = _normal((E, H, I), wl.w_std, seed_of(wl, layer, _W2, seed_base), device, dt)
     if Is > 0:
@@ -152,6 +148,16 @@ def make_layer(wl: Workload, layer: int = 0, T: int | None = None, device="cpu",
     else:
         d["shared_gate_w"] = None
     return d
+
+
+def make_router(wl: Workload, layer: int, device, seed_base: int = 0):
+    """One layer's router weights [E, H] (with the Zipf column for ``zipf``)."""
+    wr = _normal((wl.n_experts, wl.hidden), wl.router_std, seed_of(wl, layer, _WR, seed_base), device,
+                 wl.torch_dtype)
+    if wl.routing == "zipf":
+        r = torch.from_numpy(zipf_ranks(wl, layer, seed_base).astype(np.float64))
+        wr[:, 0] = (-wl.zipf_s * torch.log(r)).to(wl.torch_dtype).to(wr.device)
+    return wr
 
 
 def make_x(wl: Workload, layer: int, T: int, device, seed_base: int = 0):

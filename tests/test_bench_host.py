@@ -76,3 +76,20 @@ def test_kernel_code_hash_ignores_comments_only():
     assert bench.code_lines(src) == ['int f() {', '  return g("a//b");', '}']
     assert h(src) == h(same)
     assert h(src) != h(changed)
+
+
+def test_reference_arm_times_exactly_the_steps_it_reports(capsys):
+    """The reference arm (the oracle on the host cores) times K steps after W
+    untimed ones and reports them; its per-step time times K stays within the
+    oracle time it measured, and the record names the CPU it ran on."""
+    import argparse
+    import json
+    args = argparse.Namespace(steps=3, warmup=1, gpus=1)
+    wl = moe_synth.workload("tiny")
+    bench.run_reference(args, wl, 1, 0)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["steps"] == 3 and line["warmup"] == 1
+    cb = line["cpu_baseline"]
+    assert cb["cores"] == 1 and cb["nproc"] >= 1 and cb["cpu_model"]
+    assert "3 timed steps" in cb["sample"]
+    assert line["value"] > 0 and line["ms_per_step"] > 0
