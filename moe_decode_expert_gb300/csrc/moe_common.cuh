@@ -44,6 +44,23 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
+// Phase trace (built only with -DMOE_PHASE_TRACE, into a separate library):
+// thread 0 of each CTA stores the GPU global time at fixed points of a T = 1
+// kernel into its launch's record (kernel argument `a.trace`, [CTA][slot]),
+// read back by moe_trace_read.  Compiled out otherwise.
+#ifdef MOE_PHASE_TRACE
+constexpr int kTraceSlots = 16, kTraceCtas = 256, kTraceLaunches = 64;
+#define MOE_STAMP(s)                                                          \
+  do {                                                                        \
+    if (threadIdx.x == 0 && blockIdx.x < kTraceCtas)                          \
+      a.trace[blockIdx.x * kTraceSlots + (s)] = global_ns();                  \
+  } while (0)
+#else
+#define MOE_STAMP(s) \
+  do {               \
+  } while (0)
+#endif
+
 __device__ __forceinline__ void report_error(Control* c, uint32_t code, uint32_t detail) {
   if (atomicCAS(&c->status, 0u, code) == 0u) atomicExch(&c->detail, detail);
 }

@@ -48,21 +48,16 @@ constexpr int kDecWarps = kDecThreads / 32;
 constexpr int kChunks = 8;  // 16-byte chunks per lane per row kept in flight
 
 // Phase trace (built only with -DMOE_PHASE_TRACE, into a separate library):
-// thread 0 of each CTA stores the GPU global time at fixed points of the
-// kernel into a ring of per-launch records, read back by moe_trace_read.
+// the ring of per-launch stamp records both T = 1 kernels write.
 #ifdef MOE_PHASE_TRACE
-constexpr int kTraceSlots = 16, kTraceCtas = 256, kTraceLaunches = 64;
 __device__ uint64_t g_moe_trace[kTraceLaunches * kTraceCtas * kTraceSlots];
 static std::atomic<unsigned> g_trace_next{0};  // ring position of the next launch
-#define MOE_STAMP(s)                                                          \
-  do {                                                                        \
-    if (threadIdx.x == 0 && blockIdx.x < kTraceCtas)                          \
-      a.trace[blockIdx.x * kTraceSlots + (s)] = global_ns();                  \
-  } while (0)
-#else
-#define MOE_STAMP(s) \
-  do {               \
-  } while (0)
+uint64_t* trace_next_record() {
+  void* base = nullptr;
+  if (cudaGetSymbolAddress(&base, g_moe_trace) != cudaSuccess) return nullptr;
+  return static_cast<uint64_t*>(base) +
+         static_cast<size_t>(g_trace_next++ % kTraceLaunches) * kTraceCtas * kTraceSlots;
+}
 #endif
 
 struct DecodeArgs {
@@ -943,6 +938,13 @@ static moe_status_t launch_decode_dt(const DecodeArgs& args, int G, size_t smem,
 
 moe_status_t launch_decode_fused(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws,
                                  const WsLayout& L, cudaStream_t st) {
+  // Standard shapes stream their weights by TMA (moe_decode_stream.cu); the
+  // kernel below takes every other shape.
+  if (decode_stream_ok(c)) {
+    const moe_status_t s = launch_decode_stream(c, p, ws, L, st);
+    if (s == MOE_OK) stat_decode_stream();
+    return s;
+  }
   const int G = decode_grid(c);
   DecodeArgs a;
   a.x = static_cast<const uint8_t*>(p.x);
@@ -970,13 +972,9 @@ moe_status_t launch_decode_fused(const moe_cfg_t& c, const BlockPtrs& p, uint8_t
   decode_smem_layout(c, G, a.off_xh, a.off_lg, a.off_act, a.off_terms, a.off_w2, smem);
   a.timeout_ns = wait_timeout_ns();
 #ifdef MOE_PHASE_TRACE
-  {
-    void* base = nullptr;
-    if (cudaGetSymbolAddress(&base, g_moe_trace) != cudaSuccess) return check_launch("trace buffer");
-    a.trace = static_cast<uint64_t*>(base) +
-              static_cast<size_t>(g_trace_next++ % kTraceLaunches) * kTraceCtas * kTraceSlots;
-    if (G > kTraceCtas) return set_error(MOE_ERR_UNSUPPORTED, "trace build: more than %d CTAs", kTraceCtas);
-  }
+  a.trace = trace_next_record();
+  if (!a.trace) return check_launch("trace buffer");
+  if (G > kTraceCtas) return set_error(MOE_ERR_UNSUPPORTED, "trace build: more than %d CTAs", kTraceCtas);
 #endif
   if (smem > 227 * 1024)
     return set_error(MOE_ERR_UNSUPPORTED, "decode: needs %zu B of shared memory per CTA (max 232448)", smem);
