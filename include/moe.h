@@ -60,7 +60,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 3
+#define MOE_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define MOE_API __attribute__((visibility("default")))
@@ -134,8 +134,6 @@ typedef struct moe_stats {
   uint64_t kernels_launched;     /* every kernel this library enqueued          */
   uint64_t decode_general_calls; /* T == 1 calls on the all-paths decode kernel
                                     (shapes outside the specialised ones)       */
-  uint64_t decode_stream_calls;  /* T == 1 calls on the TMA-streaming decode
-                                    kernel (the standard shapes)                */
 } moe_stats_t;
 
 /* ABI version of the loaded library (MOE_ABI_VERSION it was built with). */
@@ -212,7 +210,7 @@ MOE_API moe_status_t moe_grouped_forward(const moe_cfg_t* cfg, const void* x, co
  * is in that array and survives later calls: moe_query_status(NULL, stream)
  * reads and clears it.  Host-side errors are returned as for every other
  * call.  Arguments as moe_decode_forward, minus the workspace. */
-#define MOE_NOALLOC_SCRATCH_BYTES (2u * 1024u * 1024u)
+#define MOE_NOALLOC_SCRATCH_BYTES (256u * 1024u)
 MOE_API moe_status_t moe_decode_forward_noalloc(const moe_cfg_t* cfg, const void* x, const void* router_w,
                                                 const void* w13, const void* w2, const void* shared_w13,
                                                 const void* shared_w2, const void* shared_gate_w,

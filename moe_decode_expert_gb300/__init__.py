@@ -52,8 +52,7 @@ class moe_topk_t(ctypes.Structure):
 
 class moe_stats_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in ("decode_fused_calls", "router_calls", "grouped_calls",
-                                               "grouped_tc_calls", "kernels_launched", "decode_general_calls",
-                                               "decode_stream_calls")]
+                                               "grouped_tc_calls", "kernels_launched", "decode_general_calls")]
 
 
 MOE_FLAG_GROUPED_SIMT = 1

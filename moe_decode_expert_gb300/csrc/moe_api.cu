@@ -31,10 +31,9 @@ moe_status_t check_launch(const char* what) {
 
 // ---------------------------------------------------------------- counters
 static std::atomic<uint64_t> g_decode{0}, g_router{0}, g_grouped{0}, g_grouped_tc{0}, g_kernels{0},
-    g_decode_general{0}, g_decode_stream{0};
+    g_decode_general{0};
 void stat_decode() { g_decode.fetch_add(1, std::memory_order_relaxed); }
 void stat_decode_general() { g_decode_general.fetch_add(1, std::memory_order_relaxed); }
-void stat_decode_stream() { g_decode_stream.fetch_add(1, std::memory_order_relaxed); }
 void stat_router() { g_router.fetch_add(1, std::memory_order_relaxed); }
 void stat_grouped() { g_grouped.fetch_add(1, std::memory_order_relaxed); }
 void stat_grouped_tc() { g_grouped_tc.fetch_add(1, std::memory_order_relaxed); }
@@ -74,14 +73,6 @@ WsLayout ws_layout(const moe_cfg_t& c, int32_t T) {
   off = align_up(off + kLogitReplicas * ((E + 2) & ~int64_t(1)) * 8, kWsAlign);
   L.ll_act = off;
   off = align_up(off + kActReplicas * ((k * I + Is + 1) & ~int64_t(1)) * 8, kWsAlign);
-  {
-    // partial-output words of the streaming decode kernel, one row of H per
-    // cluster; sized for the most clusters it ever uses (device-independent)
-    const int64_t units = (k * I + Is) / 16;
-    const int64_t cl = units < kStreamMaxClusters ? units : kStreamMaxClusters;
-    L.ll_part = off;
-    off = align_up(off + static_cast<size_t>(cl > 0 ? cl : 0) * H * 8, kWsAlign);
-  }
   L.r_logits = off;
   off = align_up(off + static_cast<size_t>(T) * (E + 1) * 4, kWsAlign);
   L.r_part = off;
@@ -328,7 +319,6 @@ moe_status_t moe_get_stats(moe_stats_t* stats) {
   stats->grouped_tc_calls = g_grouped_tc.load();
   stats->kernels_launched = g_kernels.load();
   stats->decode_general_calls = g_decode_general.load();
-  stats->decode_stream_calls = g_decode_stream.load();
   return MOE_OK;
 }
 
@@ -339,7 +329,6 @@ void moe_reset_stats(void) {
   g_grouped_tc = 0;
   g_kernels = 0;
   g_decode_general = 0;
-  g_decode_stream = 0;
 }
 
 moe_status_t moe_set_wait_timeout_ns(uint64_t ns) {

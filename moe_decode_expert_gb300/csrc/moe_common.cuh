@@ -49,7 +49,7 @@ __device__ __forceinline__ uint64_t global_ns() {
 // kernel into its launch's record (kernel argument `a.trace`, [CTA][slot]),
 // read back by moe_trace_read.  Compiled out otherwise.
 #ifdef MOE_PHASE_TRACE
-constexpr int kTraceSlots = 16, kTraceCtas = 256, kTraceLaunches = 64;
+constexpr int kTraceSlots = 32, kTraceCtas = 256, kTraceLaunches = 64;
 #define MOE_STAMP(s)                                                          \
   do {                                                                        \
     if (threadIdx.x == 0 && blockIdx.x < kTraceCtas)                          \

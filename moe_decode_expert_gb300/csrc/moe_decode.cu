@@ -938,13 +938,6 @@ static moe_status_t launch_decode_dt(const DecodeArgs& args, int G, size_t smem,
 
 moe_status_t launch_decode_fused(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws,
                                  const WsLayout& L, cudaStream_t st) {
-  // Standard shapes stream their weights by TMA (moe_decode_stream.cu); the
-  // kernel below takes every other shape.
-  if (decode_stream_ok(c)) {
-    const moe_status_t s = launch_decode_stream(c, p, ws, L, st);
-    if (s == MOE_OK) stat_decode_stream();
-    return s;
-  }
   const int G = decode_grid(c);
   DecodeArgs a;
   a.x = static_cast<const uint8_t*>(p.x);

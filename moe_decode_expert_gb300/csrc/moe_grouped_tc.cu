@@ -819,23 +819,6 @@ static bool make_map(CUtensorMap* m, int dtype, const void* base, uint64_t inner
   return r == CUDA_SUCCESS;
 }
 
-bool tma_encoder_available() { return encode_fn() != nullptr; }
-
-bool encode_map_2d(CUtensorMap* m, int dtype, const void* base, uint64_t inner, uint64_t outer, uint64_t row_stride,
-                   uint32_t box_inner, uint32_t box_rows) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {row_stride};
-  cuuint32_t box[2] = {box_inner, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  const CUresult r = fn(m, dtype == MOE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-                        const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 bool tc_shape_ok(const moe_cfg_t& c) {
   return c.dtype == MOE_BF16 && c.hidden % 128 == 0 && c.inter % 64 == 0 && c.shared_inter % 64 == 0;
 }

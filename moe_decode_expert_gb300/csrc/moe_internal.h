@@ -2,7 +2,6 @@
 // units: workspace layout, launch helpers, error reporting and counters.
 #pragma once
 
-#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -27,7 +26,6 @@ struct WsLayout {
   // single-launch decode (T == 1): exchange words between CTAs
   size_t ll_logits = 0;   // kLogitReplicas x (E + 1) words of 8 B, each copy padded to even
   size_t ll_act = 0;      // kActReplicas x (k*I + Is) words, each copy padded to even
-  size_t ll_part = 0;     // streaming decode: partial-output words [clusters][H]
   // router for T tokens
   size_t r_logits = 0;    // [T, E + 1] fp32 (column E: shared-gate logit)
   size_t r_part = 0;      // T <= 64: [H / 256 + 1, T, E + 1] fp32 split partial logits
@@ -73,7 +71,6 @@ moe_status_t check_launch(const char* what);
 // Process-wide counters.
 void stat_decode();
 void stat_decode_general();
-void stat_decode_stream();
 void stat_router();
 void stat_grouped();
 void stat_grouped_tc();
@@ -163,24 +160,6 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
-
-// The driver's tensor-map encoder could be loaded.
-bool tma_encoder_available();
-// 2-D tensor map (no swizzle) over `outer` rows of `inner` 2-byte elements,
-// rows `row_stride` bytes apart; box of box_inner x box_rows.  False if the
-// driver's encoder is unavailable or rejects the map.
-bool encode_map_2d(CUtensorMap* m, int dtype, const void* base, uint64_t inner, uint64_t outer, uint64_t row_stride,
-                   uint32_t box_inner, uint32_t box_rows);
-
-// Streaming T = 1 decode kernel (moe_decode_stream.cu): eligibility for cfg c
-// and launch.  Shapes it does not take run the general single-launch kernel.
-bool decode_stream_ok(const moe_cfg_t& c);
-moe_status_t launch_decode_stream(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws, const WsLayout& L,
-                                  cudaStream_t st);
-// Clusters (CTA pairs) the streaming kernel uses for cfg c (0 = not eligible).
-int decode_stream_clusters(const moe_cfg_t& c);
-// Upper bound on those clusters, independent of the device (workspace sizing).
-constexpr int kStreamMaxClusters = 96;
 
 #ifdef MOE_PHASE_TRACE
 // Trace build: the stamp record of the next T = 1 launch (ring of launches).

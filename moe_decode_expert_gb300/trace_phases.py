@@ -25,23 +25,6 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-# stamps of the TMA-streaming kernel (standard shapes)
-STREAM_EVENTS = [
-    "entry",
-    "PDL wait released",
-    "x staged",
-    "router rows published",
-    "logits gathered (warp 0)",
-    "ranked",
-    "routing weights ready",
-    "first stage done (warp 0)",
-    "stages done (warp 0)",
-    "partials published (warp 0)",
-    "partials gathered",
-    "output written",
-]
-
-# stamps of the general kernel (other shapes)
 EVENTS = [
     "entry",
     "PDL wait released",
@@ -96,14 +79,12 @@ def trace(workload: str, layers: int, replays: int, static_weights: bool = True)
             m.moe_decode_forward(cfg, g["x"], g["router_w"], g["w13"], g["w2"], g["shared_w13"],
                                  g["shared_w2"], g["shared_gate_w"], ids[l], wts[l], outs[l], ws, st)
 
-    m.moe_reset_stats()
     with torch.cuda.stream(st):
         step()
     torch.cuda.synchronize()
     m.moe_query_status(ws, st)
-    stream_kernel = m.moe_get_stats()["decode_stream_calls"] == layers
-    events = STREAM_EVENTS if stream_kernel else EVENTS
-    last = len(events) - 1  # "output written"
+    events = dict(enumerate(EVENTS))
+    last = len(EVENTS) - 1  # "output written"
     if lib.moe_trace_reset() != 0:
         raise RuntimeError("moe_trace_reset failed")
     graph = torch.cuda.CUDAGraph()
@@ -124,14 +105,20 @@ def trace(workload: str, layers: int, replays: int, static_weights: bool = True)
     per_launch = []
     for l in range(1, layers):
         ref = rec[l - 1, :, last].max()
-        rel = (rec[l] - ref) / 1e3  # us
-        per_launch.append((np.median(rel, axis=0), rel.max(axis=0)))
-    med = np.median(np.stack([p[0] for p in per_launch]), axis=0)
-    late = np.median(np.stack([p[1] for p in per_launch]), axis=0)
-    for e, name in enumerate(events):
-        rows.append({"event": name, "median_cta_us": float(med[e]), "last_cta_us": float(late[e])})
+        rel = np.where(rec[l] != 0, (rec[l] - ref) / 1e3, np.nan)  # us; nan where not stamped
+        with np.errstate(all="ignore"):
+            per_launch.append((np.nanmedian(rel, axis=0), np.nanmax(rel, axis=0)))
+    with np.errstate(all="ignore"):
+        med = np.nanmedian(np.stack([p[0] for p in per_launch]), axis=0)
+        late = np.nanmedian(np.stack([p[1] for p in per_launch]), axis=0)
+    for e, name in sorted(events.items()):
+        have = rec[1:, :, e] != 0
+        if not have.any():
+            continue  # not stamped on this shape
+        rows.append({"event": name, "median_cta_us": float(med[e]), "last_cta_us": float(late[e]),
+                     "ctas": int(have[0].sum())})
     span = [float((rec[l, :, last].max() - rec[l - 1, :, last].max()) / 1e3) for l in range(1, layers)]
-    return {"workload": workload, "kernel": "decode_stream_kernel" if stream_kernel else "decode_fused_kernel",
+    return {"workload": workload, "kernel": "decode_fused_kernel",
             "layers": layers, "replays": replays, "ctas": int(used.sum()),
             "static_weights": static_weights, "layer_us_median": float(np.median(span)), "events": rows}
 
@@ -147,9 +134,9 @@ def main():
     r = trace(a.workload, a.layers, a.replays, not a.no_static_weights)
     print(f"{r['workload']} ({r['kernel']}): {r['ctas']} CTAs, {r['layers']} chained layers, median layer "
           f"{r['layer_us_median']:.2f} us (last output to last output)")
-    print(f"{'us after the previous layer ends':>34} | {'median CTA':>10} | {'last CTA':>9}")
+    print(f"{'us after the previous layer ends':>34} | {'median CTA':>10} | {'last CTA':>9} | CTAs")
     for e in r["events"]:
-        print(f"{e['event']:>34} | {e['median_cta_us']:10.2f} | {e['last_cta_us']:9.2f}")
+        print(f"{e['event']:>34} | {e['median_cta_us']:10.2f} | {e['last_cta_us']:9.2f} | {e['ctas']}")
     if a.json:
         with open(a.json, "w") as f:
             json.dump(r, f, indent=1)
