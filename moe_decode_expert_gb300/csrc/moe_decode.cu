@@ -27,7 +27,7 @@
 //            into padded shared-memory rows.
 //   phase 4  after an arrival counter shows every CTA's activations out, each
 //            warp gathers the activations of its column range, splits them
-//            into three storage-type terms and runs m16n8k16 steps over its
+//            into two storage-type terms and runs m16n8k16 steps over its
 //            W2 columns: out[h] = sum_j w_j (W2_j act_j) + g (Ws2 sact) for
 //            this CTA's output rows, the warps' partial rows summed in order.
 // Each exchange wait is bounded by the GPU global timer and records an
@@ -244,14 +244,15 @@ __device__ __forceinline__ void gemv_store_partials(float (*part)[64], int warp,
   }
 }
 
-// v = t0 + t1 + t2 in the storage type: t0 = rn(v), t1 = rn(v - t0),
-// t2 = rn(v - t0 - t1) (both differences are exact in fp32): about 24
-// significant bits in bf16.  term[s] packs term s of v.x (low half) and v.y.
+// v ~ t0 + t1 in the storage type: t0 = rn(v), t1 = rn(v - t0) (the
+// difference is exact in fp32): about 16 significant bits in bf16, 22 in fp16
+// (the unit roundoff of the pair is 2^-17 and 2^-22, far inside the block's
+// tolerance).  term[s] packs term s of v.x (low half) and v.y.
 template <int DT>
-__device__ __forceinline__ void split3(float2 v, uint32_t (&term)[3]) {
+__device__ __forceinline__ void split2(float2 v, uint32_t (&term)[2]) {
   float x = v.x, y = v.y;
 #pragma unroll
-  for (int s = 0; s < 3; ++s) {
+  for (int s = 0; s < 2; ++s) {
     uint32_t bx, by;
     float rx, ry;
     if constexpr (DT == MOE_BF16) {
@@ -651,22 +652,24 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
   // ---- phase 4 (per warp): this warp's activations and W2 columns
   // The warp reads the exchange words of its columns (all requested at once,
   // re-polling any not yet published) into its range of `acts`, writes the
-  // three storage-type terms of each activation (split3; the routed ones
+  // two storage-type terms of each activation (split2; the routed ones
   // already weighted, the shared ones times the gate here; fp16 scaled by a
   // power of two that puts the range's largest magnitude in [2^14, 2^15),
   // exact and undone on the sums) in B-fragment order, then runs its
   // tensor-core steps: out[h0 + r] = sum over the K columns of W2 row r times
   // the activations, A = 16 W2 rows x 16 columns (ldmatrix from the padded
-  // rows), B columns 0-2 = the activation terms, fp32 accumulation.  Lane t of
+  // rows), B columns 0-1 = the activation terms, fp32 accumulation.  Lane t of
   // a B fragment needs columns 2t, 2t+1, 2t+8, 2t+9 of a step, kept at
   // 4t..4t+3 of the step's 16 slots.
-  // One thread per CTA counts CTAs in and waits for all G of them before any
-  // warp reads the activation words: every warp polling the words while other
-  // CTAs are still producing floods L2 with re-reads and slows the weight
-  // streams.  After the count the words have (nearly always) landed and each
-  // warp's gather is one round trip (the epoch tags still catch a late one).
-  // A CTA counts itself in as soon as its activations are out; its own W2
-  // copies land while it waits.
+  // One thread per CTA counts CTAs in and waits until 5/8 of them have
+  // arrived before any warp reads the activation words: every warp polling the
+  // words while most CTAs are still producing floods L2 with re-reads and
+  // slows the weight streams, while waiting for all G puts a full round trip
+  // after the last arrival.  From 5/8 on, the gather's first round trip
+  // overlaps the last CTAs' work and the epoch tags make it re-poll the words
+  // not yet published (measured: 5/8 and 1/2 equally best, 1/4 and all G
+  // slower).  A CTA counts itself in as soon as its activations are out; its
+  // own W2 copies land while it waits.
   MOE_STAMP(8);  // thread 0's phase-3 work done
   __syncthreads();
   if (tid == 0 && !s_fail) {
@@ -674,11 +677,11 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
     atomicAdd(cnt, 1u);
     const uint64_t deadline = global_ns() + a.timeout_ns;
     bool arrived = true;
-    while (ld_relaxed_u32(cnt) < static_cast<uint32_t>(G)) {
+    while (ld_relaxed_u32(cnt) < static_cast<uint32_t>((G * 5) / 8)) {
       if (global_ns() > deadline) { arrived = false; break; }
     }
     if (!arrived) s_fail = kDevTimeoutAct;
-    MOE_STAMP(9);  // every CTA counted in
+    MOE_STAMP(9);  // 5/8 of the CTAs counted in
   }
   cp_async_wait_all();  // this thread's W2 copies
   __syncthreads();
@@ -723,19 +726,19 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
         const int pcol = 2 * qp;
         const float2 v0 = acts2[min(qp, (K >> 1) - 1)];  // clamped load, no branch
         const float f = pcol < K ? (pcol >= P ? gate : 1.0f) * sc : 0.0f;
-        uint32_t tm[3];
-        split3<DT>(make_float2(v0.x * f, v0.y * f), tm);
+        uint32_t tm[2];
+        split2<DT>(make_float2(v0.x * f, v0.y * f), tm);
         const int w = pcol & 15;
         const int at = (pcol & ~15) + (w < 8 ? 2 * w : 2 * w - 14);
 #pragma unroll
-        for (int e = 0; e < 3; ++e) *reinterpret_cast<uint32_t*>(terms + static_cast<size_t>(e) * Kp + at) = tm[e];
+        for (int e = 0; e < 2; ++e) *reinterpret_cast<uint32_t*>(terms + static_cast<size_t>(e) * Kp + at) = tm[e];
       }
     }
     __syncwarp();  // terms and this warp's W2 copies visible to all its lanes
     MOE_STAMP(12);  // terms written
     const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8;
     const uint32_t ta0 = smem_u32(terms) + static_cast<uint32_t>(g * Kp + 4 * t) * 2;
-    const bool bl = lane < 12;  // lanes holding B columns 0-2
+    const bool bl = lane < 8;  // lanes holding B columns 0-1
     float acc[4][4], acc1[4];
 #pragma unroll
     for (int m = 0; m < 4; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.0f;
@@ -799,7 +802,7 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
         }
       }
     }
-    // columns 0, 1 (lane t = 0) and 2 (lane t = 1) of rows g and g + 8
+    // columns 0 and 1 (lane t = 0; the other columns are zero) of rows g and g + 8
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       float top = acc[m][0] + acc[m][1], bot = acc[m][2] + acc[m][3];
@@ -867,7 +870,7 @@ static void decode_smem_layout(const moe_cfg_t& c, int G, uint32_t& off_xh, uint
   off_act = static_cast<uint32_t>(off);
   off += align_up((Kp + 2) * 4, 128);
   off_terms = static_cast<uint32_t>(off);
-  off += align_up(3 * Kp * 2, 128);
+  off += align_up(2 * Kp * 2, 128);
   off_w2 = static_cast<uint32_t>(off);
   off += align_up(hn_max * (k * w2_row_stride(c.inter) + (Is ? w2_row_stride(c.shared_inter) : 0)), 128);
   total = off;

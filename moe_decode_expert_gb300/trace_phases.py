@@ -35,7 +35,7 @@ EVENTS = [
     "ranked",
     "routing weights ready (warp 0)",
     "phase-3 work done (thread 0)",
-    "every CTA counted in (thread 0)",
+    "5/8 of the CTAs counted in (thread 0)",
     "W2 copies landed",
     "activations gathered (warp 0)",
     "terms written (warp 0)",
