@@ -156,7 +156,7 @@ MOE_API moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, void* stream)
  *   logits (optional, may be NULL) [T, E] fp32 receives the raw router logits.
  * Ranking key: fp32 logit, descending; equal logits rank the lower expert
  * index first.  Weights: fp32 softmax over all E, then renormalised over the
- * k when cfg->norm_topk. */
+ * k when cfg->norm_topk.  T == 0 validates cfg only and enqueues nothing. */
 MOE_API moe_status_t moe_router_topk(const moe_cfg_t* cfg, const void* x, const void* router_w, int32_t T,
                              moe_topk_t topk, float* logits, void* ws, size_t ws_bytes, void* stream);
 
@@ -183,7 +183,9 @@ MOE_API moe_status_t moe_decode_forward(const moe_cfg_t* cfg, const void* x, con
  * synchronisation) so each selected expert's weights stream from HBM once per
  * tile of its tokens, then combines per token in slot order.
  * ("Decode throughput analysis report", code-level profiling section.)
- * Arguments as moe_decode_forward, with x [T, H], out [T, H], topk [T, k]. */
+ * Arguments as moe_decode_forward, with x [T, H], out [T, H], topk [T, k].
+ * T == 0 validates cfg only and enqueues nothing (the per-token buffers may
+ * then be NULL). */
 MOE_API moe_status_t moe_grouped_forward(const moe_cfg_t* cfg, const void* x, const void* router_w,
                                  const void* w13, const void* w2, const void* shared_w13,
                                  const void* shared_w2, const void* shared_gate_w, moe_topk_t topk,

@@ -230,11 +230,11 @@ moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, void* stream) {
 moe_status_t moe_router_topk(const moe_cfg_t* cfg, const void* x, const void* router_w, int32_t T,
                              moe_topk_t topk, float* logits, void* ws, size_t ws_bytes, void* stream) {
   if (moe_status_t s = check_cfg(cfg)) return s;
+  if (T < 0) return set_error(MOE_ERR_INVALID_ARG, "T must be >= 0");
+  if (T == 0) return MOE_OK;  // nothing to do; the per-token buffers may be empty (NULL)
   if (moe_status_t s = check_ptr(x, "x")) return s;
   if (moe_status_t s = check_ptr(router_w, "router_w")) return s;
   if (!topk.ids || !topk.weights) return set_error(MOE_ERR_INVALID_ARG, "topk.ids / topk.weights is NULL");
-  if (T < 0) return set_error(MOE_ERR_INVALID_ARG, "T must be >= 0");
-  if (T == 0) return MOE_OK;
   WsLayout L;
   if (moe_status_t s = check_ws(*cfg, ws, ws_bytes, T, L)) return s;
   // The router-only entry ranks the E routed experts; the gate column is not needed.
@@ -266,10 +266,10 @@ moe_status_t moe_grouped_forward(const moe_cfg_t* cfg, const void* x, const void
                                  const void* w2, const void* shared_w13, const void* shared_w2,
                                  const void* shared_gate_w, moe_topk_t topk, void* out, void* ws,
                                  size_t ws_bytes, int32_t T, void* stream) {
+  if (T < 0) return set_error(MOE_ERR_INVALID_ARG, "T must be >= 0");
+  if (T == 0) return check_cfg(cfg);  // nothing to do; the per-token buffers may be empty (NULL)
   if (moe_status_t s = check_block(cfg, x, router_w, w13, w2, shared_w13, shared_w2, shared_gate_w, topk, out))
     return s;
-  if (T < 0) return set_error(MOE_ERR_INVALID_ARG, "T must be >= 0");
-  if (T == 0) return MOE_OK;
   WsLayout L;
   if (moe_status_t s = check_ws(*cfg, ws, ws_bytes, T, L)) return s;
   BlockPtrs p{x, router_w, w13, w2, shared_w13, shared_w2, shared_gate_w, topk.ids, topk.weights, out};

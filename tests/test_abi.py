@@ -129,6 +129,16 @@ def test_zero_tokens_is_a_no_op(m):
     rc = lib.moe_grouped_forward(ctypes.byref(c), vp(256), vp(512), vp(768), vp(1024), None, None, None,
                                  _topk(m), vp(2048), None, 0, 0, None)
     assert rc == 0
+    # with no tokens the per-token buffers may be NULL; the cfg is still checked
+    rc = lib.moe_grouped_forward(ctypes.byref(c), None, vp(512), vp(768), vp(1024), None, None, None,
+                                 m.moe_topk_t(None, None), None, None, 0, 0, None)
+    assert rc == 0
+    bad = m.MoeCfg(256, 16, 2, 60, 0, m.MOE_F16).c()
+    rc = lib.moe_grouped_forward(ctypes.byref(bad), None, None, None, None, None, None, None,
+                                 m.moe_topk_t(None, None), None, None, 0, 0, None)
+    assert rc == 2
+    rc = lib.moe_router_topk(ctypes.byref(c), None, None, 0, m.moe_topk_t(None, None), None, None, 0, None)
+    assert rc == 0
 
 
 def test_timeout_setting(m):

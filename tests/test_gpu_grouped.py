@@ -221,3 +221,51 @@ def test_residual_flag_grouped(m, flags):
     assert torch.equal(o1, o0 + g["x"].float())
     _, _, o2 = _grouped(m, wl, g, T, flags=flags | 8)
     assert torch.equal(o2, o1.to(torch.bfloat16))
+
+
+@pytest.mark.parametrize("flags", [SIMT, TC], ids=["simt", "tcgen05"])
+def test_no_renormalisation_no_shared_expert(m, flags):
+    """norm_topk = 0 (full-softmax weights) and no shared expert on both T > 1
+    paths, every token against the oracle."""
+    wl = moe_synth.Workload("nonorm", 512, 64, 6, 128, 0, moe_synth.BF16, 0, 1.0, 0.05, 0.05, norm_topk=0,
+                            preset_id=11)
+    T = 24
+    d = moe_synth.make_layer(wl, 0, T)
+    g = {k_: (v.to(DEV) if v is not None else None) for k_, v in d.items()}
+    ids, w, out = _grouped(m, wl, g, T, out_dtype=3, flags=flags)
+    ref = oracle_full(wl, d)
+    good = min_rank_gap(ref["logits"], wl.top_k) > 1e-4
+    assert good.sum() >= T // 2
+    assert np.array_equal(ids.cpu().numpy()[good], ref["ids"][good])
+    np.testing.assert_allclose(w.cpu().numpy()[good], ref["w"][good], rtol=1e-4, atol=1e-7)
+    assert np.all(w.sum(-1).cpu().numpy() < 1.0)  # full-softmax weights of k of E experts
+    parity(out, ref["out"])
+
+
+def test_fp16_batches_take_the_cuda_core_path(m):
+    """fp16 with T > 1 runs the CUDA-core grouped kernels (the tensor-core
+    passes are bf16 only) and matches the oracle on every token."""
+    wl = moe_synth.workload("sharded_decode")
+    T = 6
+    g = moe_synth.make_layer(wl, 3, T, device=DEV)
+    m.moe_reset_stats()
+    ids, w, out = _grouped(m, wl, g, T)
+    st = m.moe_get_stats()
+    assert st["grouped_calls"] == 1 and st["grouped_tc_calls"] == 0
+    tokens = list(range(T))
+    check_tokens(ids, w, out, oracle_tokens(wl, g, tokens), tokens, wl.top_k)
+
+
+def test_zero_tokens_is_a_no_op(m):
+    wl = moe_synth.workload("small_batch")
+    g = moe_synth.make_layer(wl, 0, 2, device=DEV)
+    cfg = m.cfg_from_workload(wl)
+    ws = m.alloc_workspace(cfg, 2, DEV)
+    x0 = g["x"][:0]
+    ids = torch.empty(0, wl.top_k, dtype=torch.int32, device=DEV)
+    w = torch.empty(0, wl.top_k, dtype=torch.float32, device=DEV)
+    out = torch.empty(0, wl.hidden, dtype=cfg.out_torch_dtype, device=DEV)
+    m.moe_reset_stats()
+    m.moe_grouped_forward(cfg, x0, g["router_w"], g["w13"], g["w2"], g["shared_w13"], g["shared_w2"],
+                          g["shared_gate_w"], ids, w, out, ws)
+    assert m.moe_get_stats()["kernels_launched"] == 0
