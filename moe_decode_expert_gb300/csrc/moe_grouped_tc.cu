@@ -712,6 +712,10 @@ __global__ void __launch_bounds__(1024) tc_schedule_kernel(const int32_t* counts
 // partial sums (every load in flight at once), warp t ranks token t, then all
 // threads group and schedule; ids, counts and offsets pass between the stages
 // in shared memory.
+// kWarp: the grouping by one warp and the tile lists by every thread (at most
+// kWarpGroupPairs pairs with the shared expert); else the CTA-wide stages.  Two
+// instantiations, so each launch carries only its own code.
+template <bool kWarp>
 __global__ void __launch_bounds__(1024) route_group_kernel(float* logits, const float* part,
                                                            int nsplit, int T, int E, int E1, int k, int norm_topk,
                                                            int32_t* ids, float* w, int has_shared, int32_t* counts,
@@ -757,9 +761,15 @@ __global__ void __launch_bounds__(1024) route_group_kernel(float* logits, const 
     if (lane < k) s_flat[warp * k + lane] = s_ids[warp][lane];
   }
   __syncthreads();
-  group_stage(s_flat, T, k, E, has_shared, counts, offsets, perm, nullptr, 0, ctrl, s_cnt, s_off);
-  __syncthreads();
-  schedule_stage(s_cnt, s_off, E, I, Is, H, N, mt13, mt2, n13, n2, t13, t2);
+  if constexpr (kWarp) {
+    // few pairs: one warp groups them, every thread lists the tiles (one
+    // barrier in between; the passes read only perm and the tile lists)
+    small_group_schedule(s_flat, T, k, E, has_shared, perm, ctrl, I, Is, H, N, mt13, mt2, n13, n2, t13, t2);
+  } else {
+    group_stage(s_flat, T, k, E, has_shared, counts, offsets, perm, nullptr, 0, ctrl, s_cnt, s_off);
+    __syncthreads();
+    schedule_stage(s_cnt, s_off, E, I, Is, H, N, mt13, mt2, n13, n2, t13, t2);
+  }
 }
 
 // Xs[pos, :] = x[token of perm[pos], :]: one warp per row, 16-byte chunks,
@@ -874,8 +884,11 @@ static moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uin
     float* lg = reinterpret_cast<float*>(ws + L.r_logits);
     const int E1 = c.has_shared_gate ? E + 1 : E;
     const size_t lg_bytes = static_cast<size_t>(T) * E1 * sizeof(float);
-    if (raise_smem_limit(route_group_kernel, lg_bytes) != cudaSuccess) return check_launch("route_group_kernel (smem)");
-    launch_pdl(route_group_kernel, dim3(1), dim3(1024), lg_bytes, st, lg, reinterpret_cast<const float*>(ws + L.r_part),
+    // the one-warp grouping wins up to T = 8 at k = 8 (measured); it needs the
+    // pairs and the shared expert's entry within kWarpGroupPairs
+    auto kern = T * k + (Is > 0 ? 1 : 0) <= kWarpGroupPairs ? route_group_kernel<true> : route_group_kernel<false>;
+    if (raise_smem_limit(kern, lg_bytes) != cudaSuccess) return check_launch("route_group_kernel (smem)");
+    launch_pdl(kern, dim3(1), dim3(1024), lg_bytes, st, lg, reinterpret_cast<const float*>(ws + L.r_part),
                fused_nsplit, T, E, E1, k, c.norm_topk, p.topk_ids, p.topk_w, Is > 0 ? 1 : 0, counts, offsets, perm,
                ctrl, I, Is, H, N, mt13, kMT, sched, sched + 1, t13, t2);
     if (moe_status_t s = check_launch("route_group_kernel")) return s;

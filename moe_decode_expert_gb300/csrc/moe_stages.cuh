@@ -257,4 +257,151 @@ __device__ __forceinline__ void schedule_stage(const int32_t* counts,
   }
 }
 
+// Small batches (T*k routed pairs plus the shared expert's entry at most
+// kWarpGroupPairs): the grouping of the pairs by expert by one warp, then the
+// tile lists by every thread after one CTA barrier (the tile-list kernels and
+// the passes read only perm and the lists).  Pair p (routed: token p / k, slot
+// p % k) gets the unique key (expert << 16) | p; its rank among all keys (rank
+// counting over shared memory) is its sorted position, so each expert's pairs
+// are filed in pair order.  Runs of equal experts in sorted order are the
+// distinct experts, in ascending order, followed by the shared expert (index
+// E, its T pairs in token order after the routed ones): the same lists the
+// CTA-wide grouping and scheduling stages build.  flat_ids: the [T, k] ids in
+// shared memory.  Called by every thread of the CTA.
+constexpr int kWarpGroupPairs = 128;
+struct WarpGroupScratch {
+  uint32_t key[kWarpGroupPairs];
+  uint32_t sorted[kWarpGroupPairs];
+  int ue[kWarpGroupPairs + 1], upos[kWarpGroupPairs + 2], pre13[kWarpGroupPairs + 2], pre2[kWarpGroupPairs + 2];
+  int nall, tot13, tot2;
+};
+__device__ __forceinline__ void small_group_schedule(const int32_t* flat_ids, int T, int k, int E, int has_shared,
+                                                     int32_t* perm, Control* ctrl, int I, int Is, int H, int N,
+                                                     int mt13, int mt2, int32_t* n13, int32_t* n2, TcTile* t13,
+                                                     TcTile* t2) {
+  constexpr int KPL = kWarpGroupPairs / 32;  // pairs per lane
+  __shared__ __align__(16) WarpGroupScratch sc;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int np = T * k;  // np + has_shared <= kWarpGroupPairs (checked by the caller)
+  if (tid < 32) {
+    uint32_t key[KPL];
+#pragma unroll
+    for (int r = 0; r < KPL; ++r) {
+      const int p = lane + 32 * r;
+      key[r] = 0xffffffffu;
+      if (p < np) {
+        int e = flat_ids[p];
+        if (e < 0 || e >= E) {
+          report_error(ctrl, kDevBadExpert, static_cast<uint32_t>(p));
+          e = 0;
+        }
+        key[r] = (static_cast<uint32_t>(e) << 16) | static_cast<uint32_t>(p);
+      }
+      sc.key[p] = key[r];
+    }
+    __syncwarp();
+    int rk[KPL];
+#pragma unroll
+    for (int r = 0; r < KPL; ++r) rk[r] = 0;
+    for (int j = 0; j < np; j += 4) {  // keys past np are all-ones: never smaller
+      const uint4 kk = *reinterpret_cast<const uint4*>(sc.key + j);  // broadcast
+#pragma unroll
+      for (int r = 0; r < KPL; ++r)
+        rk[r] += (kk.x < key[r]) + (kk.y < key[r]) + (kk.z < key[r]) + (kk.w < key[r]);
+    }
+#pragma unroll
+    for (int r = 0; r < KPL; ++r)
+      if (lane + 32 * r < np) {
+        perm[rk[r]] = static_cast<int32_t>(key[r] & 0xffffu);
+        sc.sorted[rk[r]] = key[r];
+      }
+    if (has_shared)
+      for (int t = lane; t < T; t += 32) perm[np + t] = np + t;
+    __syncwarp();
+    // distinct experts: sorted positions where the expert changes
+    int nu = 0;
+#pragma unroll
+    for (int r = 0; r < KPL; ++r) {
+      const int pos = lane + 32 * r;
+      const bool start = pos < np && (pos == 0 || (sc.sorted[pos] >> 16) != (sc.sorted[pos - 1] >> 16));
+      const uint32_t m = __ballot_sync(0xffffffffu, start);
+      if (start) {
+        const int u = nu + __popc(m & ((1u << lane) - 1u));
+        sc.ue[u] = static_cast<int>(sc.sorted[pos] >> 16);
+        sc.upos[u] = pos;
+      }
+      nu += __popc(m);
+    }
+    if (lane == 0) {
+      if (has_shared) {
+        sc.ue[nu] = E;
+        sc.upos[nu] = np;
+      }
+      sc.upos[nu + (has_shared ? 1 : 0)] = np + (has_shared ? T : 0);  // end of the last run
+    }
+    __syncwarp();
+    const int nall = nu + (has_shared ? 1 : 0);
+    // tiles of each distinct expert, then an exclusive scan (KPL entries per lane)
+    int a13[KPL], a2[KPL], s13 = 0, s2 = 0;
+#pragma unroll
+    for (int r = 0; r < KPL; ++r) {
+      const int u = KPL * lane + r;
+      a13[r] = a2[r] = 0;
+      if (u < nall) {
+        const int e = sc.ue[u], cnt = sc.upos[u + 1] - sc.upos[u];
+        const int ie = e == E ? Is : I;
+        const int nt = (cnt + N - 1) / N;
+        a13[r] = ie > 0 ? nt * ((ie / 64 + mt13 - 1) / mt13) : 0;
+        a2[r] = ie > 0 ? nt * ((H / 128 + mt2 - 1) / mt2) : 0;
+      }
+      s13 += a13[r];
+      s2 += a2[r];
+    }
+    int i13 = s13, i2 = s2;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y13 = __shfl_up_sync(0xffffffffu, i13, o), y2 = __shfl_up_sync(0xffffffffu, i2, o);
+      if (lane >= o) { i13 += y13; i2 += y2; }
+    }
+    int b13 = i13 - s13, b2 = i2 - s2;
+#pragma unroll
+    for (int r = 0; r < KPL; ++r) {
+      const int u = KPL * lane + r;
+      if (u < nall) {
+        sc.pre13[u] = b13;
+        sc.pre2[u] = b2;
+      }
+      b13 += a13[r];
+      b2 += a2[r];
+    }
+    if (lane == 31) {
+      sc.nall = nall;
+      sc.tot13 = i13;
+      sc.tot2 = i2;
+      *n13 = i13;
+      *n2 = i2;
+    }
+  }
+  __syncthreads();
+  // tile i belongs to the last distinct expert whose first tile index is <= i
+  const int nall = sc.nall, tot13 = sc.tot13, tot2 = sc.tot2;
+  for (int i = tid; i < tot13 + tot2; i += blockDim.x) {
+    const bool second = i >= tot13;
+    const int ii = second ? i - tot13 : i;
+    const int* pre = second ? sc.pre2 : sc.pre13;
+    int lo = 0, hi = nall - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pre[mid] <= ii) lo = mid; else hi = mid - 1;
+    }
+    const int e = sc.ue[lo];
+    const int ie = e == E ? Is : I;
+    const int per_n = second ? (H / 128 + mt2 - 1) / mt2 : (ie / 64 + mt13 - 1) / mt13;
+    const int j = (ii - pre[lo]) / per_n, mm = (ii - pre[lo]) - j * per_n;
+    const int cnt = sc.upos[lo + 1] - sc.upos[lo];
+    const TcTile tl{e, mm, sc.upos[lo] + j * N, min(N, cnt - j * N)};
+    if (second) t2[ii] = tl; else t13[ii] = tl;
+  }
+}
+
 }  // namespace moe
