@@ -852,6 +852,18 @@ static size_t tc_smem2() {
 // Two 128-row M-tiles per CTA: each token stage then feeds two accumulators.
 constexpr int kMT = 2;
 
+// M-tiles per W2 tile (1 or kMT).  Two share every activation stage (half the
+// activation traffic); one spreads the weights over more CTAs, which only pays
+// when it lowers the largest number of weight rows a CTA streams.  The
+// distinct experts are unknown before the routing runs, so the count is taken
+// at T*k experts (capped at E).
+static int w2_m_tiles(int T, int k, int E, int H, int sms) {
+  const int ex = (T * k < E ? T * k : E) + 1;  // with the shared expert
+  const int t1 = ex * (H / 128), t2 = ex * ((H / 128 + kMT - 1) / kMT);
+  // weight rows of the busiest CTA, in M-tiles: one M-tile per tile only if fewer
+  return (t1 + sms - 1) / sms < kMT * ((t2 + sms - 1) / sms) ? 1 : kMT;
+}
+
 template <int N>
 static moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws, const WsLayout& L,
                                      int32_t T, int fused_nsplit, cudaStream_t st) {
@@ -880,6 +892,7 @@ static moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uin
   const int sms0 = sm_count();
   const int est13 = (T * k < E ? T * k : E) * ((I / 64 + kMT - 1) / kMT);  // W13 tiles with kMT
   const int mt13 = est13 <= sms0 ? 1 : kMT;
+  const int mt2 = w2_m_tiles(T, k, E, H, sms0);
   if (fused_nsplit >= 0) {  // ranking + grouping + tile lists in one launch (small batches)
     float* lg = reinterpret_cast<float*>(ws + L.r_logits);
     const int E1 = c.has_shared_gate ? E + 1 : E;
@@ -890,10 +903,10 @@ static moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uin
     if (raise_smem_limit(kern, lg_bytes) != cudaSuccess) return check_launch("route_group_kernel (smem)");
     launch_pdl(kern, dim3(1), dim3(1024), lg_bytes, st, lg, reinterpret_cast<const float*>(ws + L.r_part),
                fused_nsplit, T, E, E1, k, c.norm_topk, p.topk_ids, p.topk_w, Is > 0 ? 1 : 0, counts, offsets, perm,
-               ctrl, I, Is, H, N, mt13, kMT, sched, sched + 1, t13, t2);
+               ctrl, I, Is, H, N, mt13, mt2, sched, sched + 1, t13, t2);
     if (moe_status_t s = check_launch("route_group_kernel")) return s;
   } else {
-    launch_pdl(tc_schedule_kernel, dim3(1), dim3(1024), 0, st, counts, offsets, E, I, Is, H, N, mt13, kMT, sched,
+    launch_pdl(tc_schedule_kernel, dim3(1), dim3(1024), 0, st, counts, offsets, E, I, Is, H, N, mt13, mt2, sched,
                sched + 1, t13, t2);
     if (moe_status_t s = check_launch("tc_schedule_kernel")) return s;
   }
@@ -926,8 +939,6 @@ static moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uin
             make_map(&mLoS, DT, alo, IsM, P, static_cast<uint64_t>(Imax) * 2, N);
   if (!ok) return set_error(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
 
-  const size_t s2 = tc_smem2<N, kMT>();
-  cudaFuncSetAttribute(tc_w2_kernel<DT, N, kMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s2));
   const int g13 = static_cast<int>(L.tc_max13 < sms ? L.tc_max13 : sms);
   const int g2 = static_cast<int>(L.tc_max2 < sms ? L.tc_max2 : sms);
   auto launch13 = [&](auto kernel, size_t s13) {
@@ -943,10 +954,13 @@ static moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uin
     else launch13(tc_w13_kernel<DT, N, kMT, false>, tc_smem13<N, kMT>());
   }
   if (moe_status_t s = check_launch("tc_w13_kernel")) return s;
-  launch_pdl(tc_w2_kernel<DT, N, kMT>, dim3(g2 > 0 ? g2 : 1), dim3(kTcThreads), s2, st, mW2, mW2s, mHi, mLo, mHiS, mLoS, t2, sched + 1,
-                                                                   perm, p.topk_w, glog, gate_stride,
-                                                                   c.has_shared_gate, T, H, I, Is, E, k, y, ctrl,
-                                                                   timeout);
+  auto launch2 = [&](auto kernel, size_t s2) {
+    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s2));
+    launch_pdl(kernel, dim3(g2 > 0 ? g2 : 1), dim3(kTcThreads), s2, st, mW2, mW2s, mHi, mLo, mHiS, mLoS, t2,
+               sched + 1, perm, p.topk_w, glog, gate_stride, c.has_shared_gate, T, H, I, Is, E, k, y, ctrl, timeout);
+  };
+  if (mt2 == 1) launch2(tc_w2_kernel<DT, N, 1>, tc_smem2<N, 1>());
+  else launch2(tc_w2_kernel<DT, N, kMT>, tc_smem2<N, kMT>());
   if (moe_status_t s = check_launch("tc_w2_kernel")) return s;
   stat_kernels(direct ? 3 : 4);
   return MOE_OK;
