@@ -212,7 +212,7 @@ MOE_API moe_status_t moe_grouped_forward(const moe_cfg_t* cfg, const void* x, co
  * is in that array and survives later calls: moe_query_status(NULL, stream)
  * reads and clears it.  Host-side errors are returned as for every other
  * call.  Arguments as moe_decode_forward, minus the workspace. */
-#define MOE_NOALLOC_SCRATCH_BYTES (256u * 1024u)
+#define MOE_NOALLOC_SCRATCH_BYTES (512u * 1024u)
 MOE_API moe_status_t moe_decode_forward_noalloc(const moe_cfg_t* cfg, const void* x, const void* router_w,
                                                 const void* w13, const void* w2, const void* shared_w13,
                                                 const void* shared_w2, const void* shared_gate_w,

@@ -305,6 +305,12 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cta = blockIdx.x, G = gridDim.x;
   const int H = a.H, E = a.E, k = a.k, I = a.I, Is = a.Is;
+  // Copies of the exchange words this instantiation writes: more copies spread
+  // the polling CTAs over more L2 lines, which pays on the wide two-pairs-per-
+  // warp shapes (full width: 19.20 -> 18.74 us) and costs on the narrow ones
+  // (sharded: 10.08 -> 10.31 us), where the extra stores sit on the chain.
+  constexpr int LREP = DEPTH == 2 ? kLogitReplicas : kLogitReplicas / 2;
+  constexpr int AREP = DEPTH == 2 ? kActReplicas : kActReplicas / 2;
   const int h0 = static_cast<int>((static_cast<long long>(H) * cta) / G);
   const int hn = static_cast<int>((static_cast<long long>(H) * (cta + 1)) / G) - h0;
   const size_t rowb = static_cast<size_t>(H) * 2;
@@ -447,9 +453,9 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
   MOE_STAMP(3);  // phase-1 dot products summed
   // Every CTA reads all logits and every activation, so each word is
   // published in several copies (readers spread over more L2 lines):
-  // eight threads per result, one copy each.
-  for (int o = tid >> 3; o < nL + nS; o += kDecThreads / 8) {
-    const int rep = tid & 7;
+  // LREP threads per result, one copy each.
+  for (int o = tid / LREP; o < nL + nS; o += kDecThreads / LREP) {
+    const int rep = tid % LREP;
     const bool logit = o < nL;
     const int pi = o - nL;
     const int ra0 = logit ? o : nL + pi, rb0 = logit ? o : nL + nS + pi;  // the two rows combined
@@ -461,9 +467,9 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
     }
     const float v = logit ? gs : silu_f(gs) * us;
     uint64_t* dst = logit ? a.ll_logits + static_cast<size_t>(rep) * a.ll_stride + cta + o * G
-                          : a.ll_act + static_cast<size_t>(rep & (kActReplicas - 1)) * a.act_stride + P +
+                          : a.ll_act + static_cast<size_t>(rep & (AREP - 1)) * a.act_stride + P +
                                 (cta + (nL + pi) * G - E1);
-    if (rep < (logit ? kLogitReplicas : kActReplicas)) ll_store(dst, v, epoch);
+    if (rep < (logit ? LREP : AREP)) ll_store(dst, v, epoch);
   }
   MOE_STAMP(4);  // phase-1 results published
 
@@ -475,7 +481,7 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
   // threads (4 threads per candidate), and candidate rank r < k fills slot r.
   if (MODE != kDecGeneral || (E <= 256 && k <= 8)) {
     if (warp == 0) {  // one warp polls the words (all warps polling floods L2)
-      const uint64_t* src = a.ll_logits + static_cast<size_t>(cta % kLogitReplicas) * a.ll_stride;
+      const uint64_t* src = a.ll_logits + static_cast<size_t>(cta % LREP) * a.ll_stride;
       const bool ok = ll_gather<8>(src, lg, E + a.has_gate, lane, 32, epoch, global_ns() + a.timeout_ns);
       if (!__all_sync(0xffffffffu, ok) && lane == 0) s_fail = kDevTimeoutLogits;
       MOE_STAMP(5);  // logits gathered
@@ -517,7 +523,7 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
     if (warp == 0) {
       // many experts or k > 8: one warp gathers all logits and ranks them
       const int nl = E + a.has_gate;
-      const uint64_t* src = a.ll_logits + static_cast<size_t>(cta % kLogitReplicas) * a.ll_stride;
+      const uint64_t* src = a.ll_logits + static_cast<size_t>(cta % LREP) * a.ll_stride;
       const bool ok = ll_gather<8>(src, lg, nl, lane, 32, epoch, global_ns() + a.timeout_ns);
       if (__all_sync(0xffffffffu, ok)) warp_topk<32>(lg, E, k, s_ids, s_sel);
       else if (lane == 0) s_fail = kDevTimeoutLogits;
@@ -581,7 +587,7 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
       if (lane == 0) s_fail = kDevTimeoutLogits;
       return false;
     }
-    if (lane < kActReplicas) ll_store(a.ll_act + static_cast<size_t>(lane) * a.act_stride + p, silu_f(g) * up * s_w[r.j], epoch);
+    if (lane < AREP) ll_store(a.ll_act + static_cast<size_t>(lane) * a.act_stride + p, silu_f(g) * up * s_w[r.j], epoch);
     return true;
   };
   if constexpr (DEPTH == 1) {
@@ -608,8 +614,8 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
       }
       gemv_store_partials(s_red, warp, lane, 0, acc);
       __syncthreads();
-      for (int o = tid >> 2; o < np3; o += kDecThreads / 4) {
-        const int rep = tid & 3;
+      for (int o = tid / AREP; o < np3; o += kDecThreads / AREP) {
+        const int rep = tid % AREP;
         float gs = 0.0f, us = 0.0f;
 #pragma unroll
         for (int w = 0; w < kDecWarps; ++w) {
@@ -618,7 +624,7 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
         }
         const int p = o * G + cta;
         const int j = min(p / I, k - 1);
-        if (rep < kActReplicas)
+        if (rep < AREP)
           ll_store(a.ll_act + static_cast<size_t>(rep) * a.act_stride + p, silu_f(gs) * us * s_w[j], epoch);
       }
     } else if (warp == 0) {
@@ -692,7 +698,7 @@ __global__ void __launch_bounds__(kDecThreads, 3 - DEPTH) decode_fused_kernel(co
     const int Kp = ksteps * 16;
     bool ok = __all_sync(0xffffffffu, s_fail == 0);  // warp-uniform
     if (ok && c1 > c0) {
-      const uint64_t* rep = a.ll_act + static_cast<size_t>(cta % kActReplicas) * a.act_stride + c0;
+      const uint64_t* rep = a.ll_act + static_cast<size_t>(cta % AREP) * a.act_stride + c0;
       const uint64_t dl = global_ns() + a.timeout_ns;
       bool got;
       if constexpr (MODE == kDecNarrow) got = ll_gather<4>(rep, acts + c0, c1 - c0, lane, 32, epoch, dl);

@@ -14,10 +14,11 @@ namespace moe {
 
 constexpr size_t kWsAlign = 256;
 // Copies of the router-logit exchange words of the single-launch decode (each
-// CTA reads one copy, so fewer CTAs poll each L2 line).
-constexpr int kLogitReplicas = 8;
-// Copies of the activation exchange words (each CTA reads one copy).
-constexpr int kActReplicas = 4;
+// CTA reads one copy, so fewer CTAs poll each L2 line): the most any
+// instantiation writes (the workspace holds this many).
+constexpr int kLogitReplicas = 16;
+// Copies of the activation exchange words (each CTA reads one copy): the most.
+constexpr int kActReplicas = 8;
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Byte offsets of every region of one workspace, for `T` tokens of a cfg.
