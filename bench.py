@@ -535,8 +535,14 @@ def grouped_stack(m, wl, T, layers, dev, steps, warmup, repeats, xs=None):
     med, _ = timed_replays([gph], stream, steps, repeats)
     m.moe_query_status(ws, stream)
     distinct = [int(torch.unique(ids[l]).numel()) for l in range(L)]
-    path = "tcgen05" if stats["grouped_tc_calls"] else ("cuda-core" if stats["grouped_calls"] else "decode")
-    return med, stats["kernels_launched"] // L, path, distinct
+    kpl = stats["kernels_launched"] // L
+    if stats["grouped_tc_calls"]:
+        path = "tcgen05"
+    elif stats["grouped_calls"]:
+        path = "single-launch batch kernel" if kpl == 1 else "cuda-core"
+    else:
+        path = "decode"
+    return med, kpl, path, distinct
 
 
 def run_workloads(args, m, dev, peak):

@@ -99,9 +99,12 @@ typedef struct moe_cfg {
   int32_t flags;           /* MOE_FLAG_* bits below (0 = defaults)             */
 } moe_cfg_t;
 
-/* cfg->flags bits selecting the T > 1 path.  With neither bit the library
- * picks: the tcgen05 kernels when the shape allows (bf16, H % 128 == 0, I and
- * Is multiples of 64), else the CUDA-core kernels. */
+/* cfg->flags bits selecting the T > 1 path (at most one of SIMT, TC and
+ * SINGLE).  With none of them the library picks: for 2 <= T <= 8 the
+ * single-launch kernel when the shape allows (E <= 256, top_k <= 8, H a
+ * multiple of 256 up to 2048, I and Is multiples of 16), else the tcgen05
+ * kernels when the shape allows (bf16, H % 128 == 0, I and Is multiples of
+ * 64), else the CUDA-core kernels. */
 #define MOE_FLAG_GROUPED_SIMT 1  /* T > 1 on the CUDA-core grouped kernels      */
 #define MOE_FLAG_GROUPED_TC 2    /* T > 1 on the tcgen05 grouped kernels;
                                     MOE_ERR_UNSUPPORTED if the shape does not allow it */
@@ -118,6 +121,12 @@ typedef struct moe_cfg {
                                     sum, one rounding to out_dtype), so a stack
                                     of layers chains out -> x with no extra
                                     kernel.  Both the T = 1 and T > 1 paths. */
+#define MOE_FLAG_GROUPED_SINGLE 16 /* 2 <= T <= 8 in one launch: the T = 1
+                                    kernel's design, the tokens as the
+                                    tensor-core steps' B columns and the
+                                    selected experts' union streamed once;
+                                    MOE_ERR_UNSUPPORTED if T or the shape does
+                                    not allow it */
 
 /* Caller-owned routing outputs, [T, k] each (device memory). */
 typedef struct moe_topk {

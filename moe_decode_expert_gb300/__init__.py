@@ -59,6 +59,7 @@ MOE_FLAG_GROUPED_SIMT = 1
 MOE_FLAG_GROUPED_TC = 2
 MOE_FLAG_STATIC_WEIGHTS = 4
 MOE_FLAG_RESIDUAL = 8
+MOE_FLAG_GROUPED_SINGLE = 16
 
 
 @dataclass(frozen=True)

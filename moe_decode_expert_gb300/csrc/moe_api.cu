@@ -116,6 +116,16 @@ WsLayout ws_layout(const moe_cfg_t& c, int32_t T) {
       off = align_up(off + static_cast<size_t>(P) * Imax * 2, kWsAlign);
     }
   }
+  if (batch_ws_shape_ok(c, T)) {
+    size_t lw, aw;
+    const size_t pw = batch_ws_words(c, T, lw, aw);
+    L.bt_logits = off;
+    off = align_up(off + lw * 8, kWsAlign);
+    L.bt_act = off;
+    off = align_up(off + aw * 8, kWsAlign);
+    L.bt_part = off;
+    off = align_up(off + pw * 8, kWsAlign);
+  }
   L.total = off;
   return L;
 }
@@ -136,10 +146,15 @@ static moe_status_t check_cfg(const moe_cfg_t* c) {
     return set_error(MOE_ERR_INVALID_ARG, "cfg: has_shared_gate is 0 or 1");
   if (c->has_shared_gate && c->shared_inter == 0)
     return set_error(MOE_ERR_INVALID_ARG, "cfg: a shared gate needs a shared expert");
-  if (c->flags & ~(MOE_FLAG_GROUPED_SIMT | MOE_FLAG_GROUPED_TC | MOE_FLAG_STATIC_WEIGHTS | MOE_FLAG_RESIDUAL))
+  if (c->flags & ~(MOE_FLAG_GROUPED_SIMT | MOE_FLAG_GROUPED_TC | MOE_FLAG_STATIC_WEIGHTS | MOE_FLAG_RESIDUAL |
+                   MOE_FLAG_GROUPED_SINGLE))
     return set_error(MOE_ERR_INVALID_ARG, "cfg: unknown flag bits");
-  if ((c->flags & MOE_FLAG_GROUPED_SIMT) && (c->flags & MOE_FLAG_GROUPED_TC))
-    return set_error(MOE_ERR_INVALID_ARG, "cfg: MOE_FLAG_GROUPED_SIMT and MOE_FLAG_GROUPED_TC exclude each other");
+  {
+    const int path = c->flags & (MOE_FLAG_GROUPED_SIMT | MOE_FLAG_GROUPED_TC | MOE_FLAG_GROUPED_SINGLE);
+    if (path & (path - 1))
+      return set_error(MOE_ERR_INVALID_ARG,
+                       "cfg: MOE_FLAG_GROUPED_SIMT, MOE_FLAG_GROUPED_TC and MOE_FLAG_GROUPED_SINGLE exclude each other");
+  }
   if (c->hidden % 8 || c->inter % 8 || c->shared_inter % 8)
     return set_error(MOE_ERR_UNSUPPORTED, "cfg: hidden, inter and shared_inter must be multiples of 8");
   if (c->top_k > 32 || c->top_k > c->n_experts)
@@ -281,6 +296,14 @@ moe_status_t moe_grouped_forward(const moe_cfg_t* cfg, const void* x, const void
   }
   if (static_cast<int64_t>(T) * cfg->top_k > (1 << 30))
     return set_error(MOE_ERR_UNSUPPORTED, "T * top_k too large");
+  // 2 <= T <= 8: the single-launch kernel when asked for, or by default when
+  // the shape allows it and no other T > 1 path was asked for
+  const bool other = cfg->flags & (MOE_FLAG_GROUPED_SIMT | MOE_FLAG_GROUPED_TC);
+  if ((cfg->flags & MOE_FLAG_GROUPED_SINGLE) || (!other && batch_shape_ok(*cfg, T))) {
+    if (moe_status_t s = launch_decode_batch(*cfg, p, static_cast<uint8_t*>(ws), L, T, st)) return s;
+    stat_grouped();
+    return MOE_OK;
+  }
   if (moe_status_t s = launch_grouped(*cfg, p, static_cast<uint8_t*>(ws), L, T, st)) return s;
   stat_grouped();
   return MOE_OK;

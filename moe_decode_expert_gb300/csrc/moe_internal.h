@@ -20,6 +20,8 @@ constexpr int kLogitReplicas = 16;
 // Copies of the activation exchange words (each CTA reads one copy): the most.
 constexpr int kActReplicas = 8;
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+// Most tokens of the single-launch batch kernel (2 <= T <= kBatchMaxT).
+constexpr int kBatchMaxT = 8;
 
 // Byte offsets of every region of one workspace, for `T` tokens of a cfg.
 struct WsLayout {
@@ -44,6 +46,10 @@ struct WsLayout {
   size_t tc_xs = 0;       // [P, H] x rows gathered in expert order
   size_t tc_act_hi = 0;   // [P, max(I, Is)] activation, leading term
   size_t tc_act_lo = 0;   // [P, max(I, Is)] activation, remainder term
+  // single-launch batch kernel (2 <= T <= kBatchMaxT): exchange words
+  size_t bt_logits = 0;   // kLogitReplicas x [T][E + 1 padded to even] words
+  size_t bt_act = 0;      // [T*k + 1 slots][T][max(I, Is)] words (slot T*k: shared expert)
+  size_t bt_part = 0;     // [T*k + 1 slots][T][H] words
   int tc_n = 0;           // tokens per tile (0 = path not laid out)
   int64_t tc_max13 = 0;
   int64_t tc_max2 = 0;
@@ -107,6 +113,18 @@ moe_status_t launch_router(const moe_cfg_t& c, const void* x, const void* router
 moe_status_t launch_grouped(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws, const WsLayout& L,
                             int32_t T, cudaStream_t st);
 moe_status_t launch_wait_test(uint8_t* ws, cudaStream_t st);
+
+// Single-launch kernel for 2 <= T <= kBatchMaxT (moe_batch.cu).
+// batch_ws_shape_ok: the shape conditions that lay out its workspace regions
+// (no CUDA call); batch_shape_ok: those plus the grid and shared-memory fit
+// on the current device.
+bool batch_ws_shape_ok(const moe_cfg_t& c, int32_t T);
+bool batch_shape_ok(const moe_cfg_t& c, int32_t T);
+// Exchange words of the batch kernel: returns the partial words; sets the
+// logit and activation word counts.
+size_t batch_ws_words(const moe_cfg_t& c, int32_t T, size_t& logit_words, size_t& act_words);
+moe_status_t launch_decode_batch(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws, const WsLayout& L,
+                                 int32_t T, cudaStream_t st);
 
 // Tensor-core grouped passes (moe_grouped_tc.cu).
 bool tc_shape_ok(const moe_cfg_t& c);        // shape/dtype eligibility (host only)

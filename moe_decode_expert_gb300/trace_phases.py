@@ -1,14 +1,16 @@
-"""Per-phase timeline of the single-launch T = 1 decode kernel.
+"""Per-phase timeline of the single-launch decode kernels (T = 1, and the
+batch kernel for 2 <= T <= 8 with ``--T``).
 
-Builds the phase-trace variant of the library (the same kernel, compiled with
-``-DMOE_PHASE_TRACE``: thread 0 of every CTA stores the GPU global time at
-fixed points), runs ``--layers`` layers of a T = 1 workload as one CUDA graph
-of chained launches (programmatic dependent launch, static weights, as in the
+Builds the phase-trace variant of the library (the same kernels, compiled
+with ``-DMOE_PHASE_TRACE``: thread 0 of every CTA stores the GPU global time
+at fixed points), runs ``--layers`` layers of a workload as one CUDA graph of
+chained launches (programmatic dependent launch, static weights, as in the
 benchmark), replays it, and prints for every stamp its time after the
 previous layer's last CTA wrote its output: the median CTA and the latest
 CTA, each the median over the traced launches.
 
     python -m moe_decode_expert_gb300.trace_phases --workload sharded_decode
+    python -m moe_decode_expert_gb300.trace_phases --workload small_batch --T 2
 """
 from __future__ import annotations
 
@@ -42,9 +44,31 @@ EVENTS = [
     "combine steps done (warp 0)",
     "output written",
 ]
+EVENTS_BATCH = [
+    "entry",
+    "PDL wait released",
+    "x staged",
+    "phase-1 dot products summed",
+    "phase-1 results published",
+    "logits gathered (warp 0)",
+    "ranked, union formed",
+    "phase-3 passes done",
+    "activations gathered, W2 copies landed",
+    "terms written",
+    "warp 0's units done",
+    "thread 0's outputs written",
+    "first pass's dot products done (thread 0)",
+    "second pass done",
+    "third pass done",
+    "warp 0's top-k done",
+    "every token ranked",
+    "union formed (warp 0)",
+    "warp 0's first W2 unit landed",
+    "warp 0's first W2 unit computed",
+]
 
 
-def trace(workload: str, layers: int, replays: int, static_weights: bool = True) -> dict:
+def trace(workload: str, layers: int, replays: int, static_weights: bool = True, T: int = 1) -> dict:
     from moe_decode_expert_gb300 import _build
     import moe_decode_expert_gb300 as m
     import moe_synth
@@ -63,28 +87,31 @@ def trace(workload: str, layers: int, replays: int, static_weights: bool = True)
     dev = torch.device("cuda:0")
     torch.cuda.set_device(dev)
     wl = moe_synth.workload(workload, layers=layers)
-    cfg = m.cfg_from_workload(wl, None, m.MOE_FLAG_STATIC_WEIGHTS if static_weights else 0)
+    flags = (m.MOE_FLAG_STATIC_WEIGHTS if static_weights else 0) | (m.MOE_FLAG_GROUPED_SINGLE if T > 1 else 0)
+    cfg = m.cfg_from_workload(wl, None, flags)
     H, k = wl.hidden, wl.top_k
-    lay = [moe_synth.make_layer(wl, l, 1, device=dev) for l in range(layers)]
-    outs = torch.empty(layers, 1, H, dtype=cfg.out_torch_dtype, device=dev)
-    ids = torch.empty(layers, 1, k, dtype=torch.int32, device=dev)
-    wts = torch.empty(layers, 1, k, dtype=torch.float32, device=dev)
-    ws = m.alloc_workspace(cfg, 1, dev)
+    lay = [moe_synth.make_layer(wl, l, T, device=dev) for l in range(layers)]
+    outs = torch.empty(layers, T, H, dtype=cfg.out_torch_dtype, device=dev)
+    ids = torch.empty(layers, T, k, dtype=torch.int32, device=dev)
+    wts = torch.empty(layers, T, k, dtype=torch.float32, device=dev)
+    ws = m.alloc_workspace(cfg, T, dev)
     st = torch.cuda.Stream(device=dev)
     st.wait_stream(torch.cuda.current_stream(dev))
 
     def step():
         for l in range(layers):
             g = lay[l]
-            m.moe_decode_forward(cfg, g["x"], g["router_w"], g["w13"], g["w2"], g["shared_w13"],
-                                 g["shared_w2"], g["shared_gate_w"], ids[l], wts[l], outs[l], ws, st)
+            fwd = m.moe_decode_forward if T == 1 else m.moe_grouped_forward
+            fwd(cfg, g["x"], g["router_w"], g["w13"], g["w2"], g["shared_w13"], g["shared_w2"],
+                g["shared_gate_w"], ids[l], wts[l], outs[l], ws, st)
 
     with torch.cuda.stream(st):
         step()
     torch.cuda.synchronize()
     m.moe_query_status(ws, st)
-    events = dict(enumerate(EVENTS))
-    last = len(EVENTS) - 1  # "output written"
+    names = EVENTS if T == 1 else EVENTS_BATCH
+    events = dict(enumerate(names))
+    last = len(EVENTS) - 1 if T == 1 else 11  # "output written"
     if lib.moe_trace_reset() != 0:
         raise RuntimeError("moe_trace_reset failed")
     graph = torch.cuda.CUDAGraph()
@@ -118,21 +145,24 @@ def trace(workload: str, layers: int, replays: int, static_weights: bool = True)
         rows.append({"event": name, "median_cta_us": float(med[e]), "last_cta_us": float(late[e]),
                      "ctas": int(have[0].sum())})
     span = [float((rec[l, :, last].max() - rec[l - 1, :, last].max()) / 1e3) for l in range(1, layers)]
-    return {"workload": workload, "kernel": "decode_fused_kernel",
+    return {"workload": workload, "T": T, "kernel": "decode_fused_kernel" if T == 1 else "decode_batch_kernel",
             "layers": layers, "replays": replays, "ctas": int(used.sum()),
             "static_weights": static_weights, "layer_us_median": float(np.median(span)), "events": rows}
 
 
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
-    ap.add_argument("--workload", default="sharded_decode", choices=["tiny", "sharded_decode", "full_decode"])
+    ap.add_argument("--workload", default="sharded_decode",
+                    choices=["tiny", "sharded_decode", "full_decode", "small_batch"])
+    ap.add_argument("--T", type=int, default=None, help="tokens (1, or 2..8 for the batch kernel)")
     ap.add_argument("--layers", type=int, default=16)
     ap.add_argument("--replays", type=int, default=20)
     ap.add_argument("--no-static-weights", action="store_true")
     ap.add_argument("--json", default=None, help="also write the result here")
     a = ap.parse_args()
-    r = trace(a.workload, a.layers, a.replays, not a.no_static_weights)
-    print(f"{r['workload']} ({r['kernel']}): {r['ctas']} CTAs, {r['layers']} chained layers, median layer "
+    T = a.T if a.T is not None else (2 if a.workload == "small_batch" else 1)
+    r = trace(a.workload, a.layers, a.replays, not a.no_static_weights, T)
+    print(f"{r['workload']} T = {T} ({r['kernel']}): {r['ctas']} CTAs, {r['layers']} chained layers, median layer "
           f"{r['layer_us_median']:.2f} us (last output to last output)")
     print(f"{'us after the previous layer ends':>34} | {'median CTA':>10} | {'last CTA':>9} | CTAs")
     for e in r["events"]:

@@ -60,7 +60,8 @@ def _topk(m):
 
 @pytest.mark.parametrize("field,value,code", [
     ("hidden", 0, 1), ("inter", 12, 2), ("top_k", 33, 2), ("top_k", 0, 1), ("dtype", 3, 2),
-    ("n_experts", 2000, 2), ("flags", 16, 1), ("flags", 3, 1), ("norm_topk", 2, 1),
+    ("n_experts", 2000, 2), ("flags", 32, 1), ("flags", 3, 1), ("flags", 17, 1), ("flags", 18, 1),
+    ("norm_topk", 2, 1),
 ])
 def test_bad_cfg_is_rejected_on_host(m, field, value, code):
     c = m.MoeCfg(256, 16, 2, 64, 0, m.MOE_F16).c()
@@ -160,6 +161,22 @@ def test_python_binding_checks_shapes(m):
     with pytest.raises(ValueError):
         m.moe_router_topk(cfg, x, torch.zeros(16, 256, dtype=torch.float16), torch.zeros(1, 2, dtype=torch.int32),
                           torch.zeros(1, 2), torch.zeros(16, dtype=torch.uint8))
+
+
+def test_single_launch_batch_workspace(m):
+    """2 <= T <= 8 on eligible shapes: the batch kernel's exchange words (16
+    logit copies, activations and partial rows per (slot, token), slot T*k
+    being the shared expert) are laid out; T = 9 has none of them."""
+    c = m.MoeCfg(2048, 256, 8, 512, 512, m.MOE_BF16, has_shared_gate=1)
+    for T in (2, 8):
+        slots = T * 8 + 1
+        words = 16 * T * 258 + slots * T * 512 + slots * T * 2048
+        grouped_only = m.moe_workspace_bytes(m.MoeCfg(4096, 256, 8, 512, 512, m.MOE_BF16, has_shared_gate=1), T)
+        assert m.moe_workspace_bytes(c, T) >= words * 8
+        assert grouped_only > 0  # H = 4096: no batch regions, still a valid T > 1 workspace
+    # the 8-token partial rows alone (65 slots x 8 tokens x 2048 words) outweigh
+    # everything a 9-token workspace holds
+    assert m.moe_workspace_bytes(c, 8) > m.moe_workspace_bytes(c, 9)
 
 
 def test_tensor_core_path_workspace_is_laid_out_for_bf16_shapes(m):

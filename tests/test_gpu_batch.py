@@ -1,0 +1,168 @@
+"""GPU parity of the single-launch batch kernel (2 <= T <= 8 tokens in one
+launch, MOE_FLAG_GROUPED_SINGLE and the default for those T) against the
+oracle, every token: the small-batch workload with Zipf routing, the sharded
+fp16 shapes, the tiny shapes (fewer experts than SMs), odd shapes, no shared
+expert with full-softmax weights, the residual flag, calls alternating with
+the T = 1 kernel on one workspace, and the cases it refuses."""
+import numpy as np
+import pytest
+import torch
+
+import moe_synth
+from tests._util import check_tokens, min_rank_gap, oracle_full, oracle_tokens, parity
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+SINGLE, SIMT, TC, RESIDUAL = 16, 1, 2, 8
+
+
+@pytest.fixture(scope="module")
+def m():
+    import __graft_entry__
+    __graft_entry__.build()
+    import moe_decode_expert_gb300 as mod
+    return mod
+
+
+def _run(m, wl, g, T, out_dtype=None, ws=None, flags=SINGLE):
+    cfg = m.cfg_from_workload(wl, out_dtype, flags)
+    ids = torch.full((T, wl.top_k), -1, dtype=torch.int32, device=DEV)
+    w = torch.full((T, wl.top_k), float("nan"), dtype=torch.float32, device=DEV)
+    out = torch.full((T, wl.hidden), float("nan"), dtype=cfg.out_torch_dtype, device=DEV)
+    if ws is None:
+        ws = m.alloc_workspace(cfg, T, DEV)
+    m.moe_grouped_forward(cfg, g["x"], g["router_w"], g["w13"], g["w2"], g["shared_w13"], g["shared_w2"],
+                          g["shared_gate_w"], ids, w, out, ws)
+    m.moe_query_status(ws)
+    return ids, w, out
+
+
+def _host_layer(wl, T, layer=0):
+    d = moe_synth.make_layer(wl, layer, T)
+    return d, {k_: (v.to(DEV) if v is not None else None) for k_, v in d.items()}
+
+
+@pytest.mark.parametrize("T", [2, 3, 4, 8])
+def test_small_batch_zipf_single_launch(m, T):
+    wl = moe_synth.workload("small_batch")
+    g = moe_synth.make_layer(wl, 0, T, device=DEV)
+    m.moe_reset_stats()
+    ids, w, out = _run(m, wl, g, T, flags=0)  # the default for 2 <= T <= 8
+    st = m.moe_get_stats()
+    assert st["grouped_calls"] == 1 and st["grouped_tc_calls"] == 0 and st["kernels_launched"] == 1
+    tokens = list(range(T))
+    check_tokens(ids, w, out, oracle_tokens(wl, g, tokens), tokens, wl.top_k)
+
+
+@pytest.mark.parametrize("T", [2, 5, 8])
+def test_sharded_fp16_shapes(m, T):
+    """fp16 (I = 128, shared I = 128): the activation terms are scaled by a
+    power of two per (expert, token) row."""
+    wl = moe_synth.workload("sharded_decode")
+    g = moe_synth.make_layer(wl, 1, T, device=DEV)
+    ids, w, out = _run(m, wl, g, T)
+    tokens = list(range(T))
+    check_tokens(ids, w, out, oracle_tokens(wl, g, tokens), tokens, wl.top_k)
+
+
+@pytest.mark.parametrize("T", [2, 7, 8])
+def test_tiny_shapes_fewer_experts_than_sms(m, T):
+    """16 experts, top-2, no shared expert: 16 CTAs (one logit row each).
+    Values sit near the fp16 subnormal range, so parity is taken on fp32
+    output."""
+    wl = moe_synth.workload("tiny")
+    d, g = _host_layer(wl, T)
+    ids, w, out = _run(m, wl, g, T, out_dtype=3)
+    ref = oracle_full(wl, d)
+    good = min_rank_gap(ref["logits"], wl.top_k) > 1e-5
+    assert np.array_equal(ids.cpu().numpy()[good], ref["ids"][good])
+    parity(out, ref["out"])
+
+
+@pytest.mark.parametrize("T", [3, 6])
+def test_odd_small_shapes(m, T):
+    wl = moe_synth.Workload("odd", 256, 32, 4, 64, 64, moe_synth.BF16, 1, 1.0, 0.05, 0.05, preset_id=6)
+    d, g = _host_layer(wl, T)
+    ids, w, out = _run(m, wl, g, T, out_dtype=3)
+    ref = oracle_full(wl, d)
+    good = min_rank_gap(ref["logits"], wl.top_k) > 1e-5
+    assert np.array_equal(ids.cpu().numpy()[good], ref["ids"][good])
+    parity(out, ref["out"])
+
+
+def test_no_renormalisation_no_shared_expert(m):
+    wl = moe_synth.Workload("nonorm", 512, 64, 6, 128, 0, moe_synth.BF16, 0, 1.0, 0.05, 0.05, norm_topk=0,
+                            preset_id=11)
+    T = 5
+    d, g = _host_layer(wl, T)
+    ids, w, out = _run(m, wl, g, T, out_dtype=3)
+    ref = oracle_full(wl, d)
+    good = min_rank_gap(ref["logits"], wl.top_k) > 1e-4
+    assert good.sum() >= 3
+    assert np.array_equal(ids.cpu().numpy()[good], ref["ids"][good])
+    np.testing.assert_allclose(w.cpu().numpy()[good], ref["w"][good], rtol=1e-4, atol=1e-7)
+    parity(out, ref["out"])
+
+
+def test_residual_flag(m):
+    """fp32 output: exactly fl(block(x) + x) per element; bf16 output: that sum
+    rounded once."""
+    wl = moe_synth.workload("small_batch")
+    T = 6
+    g = moe_synth.make_layer(wl, 6, T, device=DEV)
+    _, _, o0 = _run(m, wl, g, T, out_dtype=3)
+    _, _, o1 = _run(m, wl, g, T, out_dtype=3, flags=SINGLE | RESIDUAL)
+    assert torch.equal(o1, o0 + g["x"].float())
+    _, _, o2 = _run(m, wl, g, T, flags=SINGLE | RESIDUAL)
+    assert torch.equal(o2, o1.to(torch.bfloat16))
+
+
+def test_repeat_calls_are_bit_identical_and_alternate_with_t1(m):
+    """The same inputs give the same bits on every call (every output element
+    is one fixed sequence of fp32 operations), also when T = 1 decode calls
+    and batch calls alternate on one workspace (they share the epoch word and
+    the T = 1 kernel's arrival counters)."""
+    wl = moe_synth.workload("small_batch")
+    T = 4
+    g = moe_synth.make_layer(wl, 5, T, device=DEV)
+    cfg = m.cfg_from_workload(wl, None, 0)
+    ws = m.alloc_workspace(cfg, T, DEV)
+    first = _run(m, wl, g, T, ws=ws)
+    g1 = dict(g)
+    g1["x"] = g["x"][:1].contiguous()
+    ref1 = oracle_tokens(wl, g1, [0])
+    for _ in range(3):
+        i1, w1, o1 = _run(m, wl, g1, 1, ws=ws, flags=0)
+        check_tokens(i1, w1, o1, ref1, [0], wl.top_k)
+        again = _run(m, wl, g, T, ws=ws)
+        for a, b in zip(first, again):
+            assert torch.equal(a, b)
+
+
+def test_agrees_with_the_tensor_core_path(m):
+    wl = moe_synth.workload("small_batch")
+    T = 8
+    g = moe_synth.make_layer(wl, 7, T, device=DEV)
+    i1, w1, o1 = _run(m, wl, g, T, out_dtype=3)
+    i2, w2, o2 = _run(m, wl, g, T, out_dtype=3, flags=TC)
+    assert torch.equal(i1, i2)
+    # the two paths sum the router dot products in different orders
+    torch.testing.assert_close(w1, w2, rtol=1e-5, atol=0)
+    parity(o1, o2.double().cpu().numpy(), max_err_frac=1e-3, rel_l1=1e-4)
+
+
+@pytest.mark.parametrize("T", [9, 16])
+def test_refuses_more_than_8_tokens(m, T):
+    wl = moe_synth.workload("small_batch")
+    g = moe_synth.make_layer(wl, 0, T, device=DEV)
+    with pytest.raises(m.MoeError) as ei:
+        _run(m, wl, g, T)
+    assert ei.value.code == 2  # MOE_ERR_UNSUPPORTED
+
+
+def test_flags_exclude_each_other(m):
+    wl = moe_synth.workload("small_batch")
+    g = moe_synth.make_layer(wl, 0, 2, device=DEV)
+    with pytest.raises(m.MoeError) as ei:
+        _run(m, wl, g, 2, flags=SINGLE | TC)
+    assert ei.value.code == 1  # MOE_ERR_INVALID_ARG

@@ -243,13 +243,23 @@ def test_no_renormalisation_no_shared_expert(m, flags):
 
 
 def test_fp16_batches_take_the_cuda_core_path(m):
-    """fp16 with T > 1 runs the CUDA-core grouped kernels (the tensor-core
-    passes are bf16 only) and matches the oracle on every token."""
+    """fp16 with T > 8 runs the CUDA-core grouped kernels by default (the
+    tensor-core passes are bf16 only; up to 8 tokens take the single-launch
+    kernel) and matches the oracle on every token, as does an fp16 batch of 6
+    on the CUDA-core kernels."""
     wl = moe_synth.workload("sharded_decode")
-    T = 6
+    T = 12
     g = moe_synth.make_layer(wl, 3, T, device=DEV)
     m.moe_reset_stats()
     ids, w, out = _grouped(m, wl, g, T)
+    st = m.moe_get_stats()
+    assert st["grouped_calls"] == 1 and st["grouped_tc_calls"] == 0 and st["kernels_launched"] > 1
+    tokens = list(range(T))
+    check_tokens(ids, w, out, oracle_tokens(wl, g, tokens), tokens, wl.top_k)
+    T = 6
+    g = moe_synth.make_layer(wl, 3, T, device=DEV)
+    m.moe_reset_stats()
+    ids, w, out = _grouped(m, wl, g, T, flags=SIMT)
     st = m.moe_get_stats()
     assert st["grouped_calls"] == 1 and st["grouped_tc_calls"] == 0
     tokens = list(range(T))
