@@ -694,7 +694,7 @@ __global__ void __launch_bounds__(kBtBlock, 1) decode_batch_kernel(const BatchAr
     if (!__all_sync(0xffffffffu, ok) && lane == 0) s_fail = kDevTimeoutAct;
   }
   cons_sync();  // the flags are in (or a wait ran out)
-  MOE_STAMP(8);  // activations published
+  MOE_STAMP(8);  // activations published (flags in)
   const bool have_act = ranked && s_fail == 0;
   if (have_act) {
     for (int row = warp; row < nsl * T; row += kBtWarps) {

@@ -53,7 +53,7 @@ EVENTS_BATCH = [
     "logits gathered (warp 0)",
     "ranked, union formed",
     "phase-3 passes done",
-    "activations gathered, W2 copies landed",
+    "activations published (flags in)",
     "terms written",
     "warp 0's units done",
     "thread 0's outputs written",
