@@ -233,7 +233,8 @@ struct BatchArgs {
   uint32_t gs2;      // ring: bytes between 2-row groups of a W2 unit (2 max(I, Is) * 2 + 16)
   uint32_t stage;    // ring stage bytes (8 W13 rows, or two W2 units of 16 rows), 64 modulo 128
   int ns;            // ring stages
-  uint32_t off_xh, off_terms, off_ring;  // the logits of phase 2 sit at the ring's start
+  uint32_t off_terms, off_ring, off_xh, off_lg;  // x rows and logits (in the ring with x_in_ring)
+  int x_in_ring;  // 1: the x rows and logits use the ring's space until its first copy
   uint64_t timeout_ns;
 #ifdef MOE_PHASE_TRACE
   uint64_t* trace;  // this launch's record: [CTA][kTraceSlots]
@@ -266,9 +267,9 @@ __global__ void __launch_bounds__(kBtBlock, 1) decode_batch_kernel(const BatchAr
   const int SH = T * k;  // exchange slot of the shared expert
   const size_t rowb = static_cast<size_t>(H) * 2;
   const int nch = H >> 3;
-  uint8_t* xh = smem + a.off_xh;
+  uint8_t* xh = smem + a.off_xh;  // phase 1, and phase 3's B fragments
   uint8_t* ring = smem + a.off_ring;
-  float* lg = reinterpret_cast<float*>(ring);  // phases 1-2 only, before the ring's first copy
+  float* lg = reinterpret_cast<float*>(smem + a.off_lg);  // phase 2 only
   const uint32_t xha = smem_u32(xh);
   const uint32_t terms_a = smem_u32(smem + a.off_terms);
   const uint32_t ring_a = smem_u32(ring);
@@ -573,13 +574,33 @@ __global__ void __launch_bounds__(kBtBlock, 1) decode_batch_kernel(const BatchAr
   cons_sync();
   const int nU = ranked ? s_nU : 0;
   if (tid == 0) s_nU = nU;  // 0 when ranking failed: the copy-issuing warp then has nothing to do
-  asm volatile("bar.arrive 2, %0;" ::"r"(kBtBlock) : "memory");  // the copy-issuing warp may start
-  MOE_STAMP(6);  // ranked, union formed
-
-  // ---- phase 3: this CTA's range of the union's gate/up pairs
+  auto start_copies = [&]() { asm volatile("bar.arrive 2, %0;" ::"r"(kBtBlock) : "memory"); };
+  if (!a.x_in_ring) start_copies();
   const Plan pl = make_plan(nU);
   const int pb0 = pl.pb0, pb1 = pl.pb1, npass = pl.npass, ub0 = pl.ub0, ub1 = pl.ub1, n13 = pl.n13, nw2 = pl.nw2;
   const int kpw = H >> 7;  // 16-column steps per warp (H / 8 columns each)
+  // x's B fragments for this warp's 16-column steps of phase 3 (column n =
+  // token g, rows k = 2t, 2t + 1 and 2t + 8, 2t + 9 of the step), read before
+  // the ring's first copy overwrites the x rows
+  uint32_t bx[16][2];
+  auto load_bx = [&]() {
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      const bool in = npass > 0 && kk < kpw && g < T;
+      const int k0 = (warp * kpw + kk) * 16 + 2 * t4;
+      const uint32_t xa = xha + static_cast<uint32_t>(in ? g : 0) * a.xs + 2 * (in ? k0 : 0);
+      bx[kk][0] = in ? lds32(xa) : 0u;
+      bx[kk][1] = in ? lds32(xa + 16) : 0u;
+    }
+  };
+  load_bx();
+  if (a.x_in_ring) {
+    cons_sync();  // every x read is done before the ring's first copy
+    start_copies();
+  }
+  MOE_STAMP(6);  // ranked, union formed
+
+  // ---- phase 3: this CTA's range of the union's gate/up pairs
   auto wait_item = [&](int it) {  // every computing thread; bounded
     if (!mbar_wait_until(&s_full[it % a.ns], (it / a.ns) & 1, global_ns() + a.timeout_ns)) s_fail = kDevTimeoutCopy;
   };
@@ -614,17 +635,6 @@ __global__ void __launch_bounds__(kBtBlock, 1) decode_batch_kernel(const BatchAr
   // gate item (lane & 4 clear) or of the up item
   const uint32_t lm13 = static_cast<uint32_t>(lane & 3) * a.gs13 + ((lane >> 3) & 1) * rb13 + (lane >> 4) * 16;
   if (npass > 0) {
-    // x's B fragments for this warp's 16-column steps: column n = token g,
-    // rows k = 2t, 2t + 1 and 2t + 8, 2t + 9 of the step
-    uint32_t bx[16][2];
-#pragma unroll
-    for (int kk = 0; kk < 16; ++kk) {
-      const bool in = kk < kpw && g < T;
-      const int k0 = (warp * kpw + kk) * 16 + 2 * t4;
-      const uint32_t xa = xha + static_cast<uint32_t>(in ? g : 0) * a.xs + 2 * (in ? k0 : 0);
-      bx[kk][0] = in ? lds32(xa) : 0u;
-      bx[kk][1] = in ? lds32(xa + 16) : 0u;
-    }
     for (int q = 0; q < npass; ++q) {
       float acc[2][4] = {};
       wait_item(2 * q);
@@ -845,7 +855,7 @@ __global__ void __launch_bounds__(kBtBlock, 1) decode_batch_kernel(const BatchAr
       for (int j = 0; j < 8; ++j)
         if (j < k) sum += __uint_as_float(static_cast<uint32_t>(wv[j]));
       if (Is > 0) sum += s_gate[tk] * __uint_as_float(static_cast<uint32_t>(wv[8]));
-      if (a.residual) sum += load_scalar<DT>(xh + static_cast<size_t>(tk) * a.xs, h);  // x, exact in fp32
+      if (a.residual) sum += load_scalar<DT>(a.x + static_cast<size_t>(tk) * rowb, h);  // x, exact in fp32
       store_out(a.out, static_cast<size_t>(tk) * H + h, sum, a.out_dtype);
     }
   }
@@ -860,7 +870,8 @@ namespace {
 struct BatchGeom {
   int G = 0, Lst = 0, Imax = 0, ns = 0;
   uint32_t xs = 0, cs = 0, gs13 = 0, gs2 = 0, stage = 0;
-  uint32_t off_xh = 0, off_terms = 0, off_ring = 0;
+  uint32_t off_terms = 0, off_ring = 0, off_xh = 0, off_lg = 0;
+  bool x_in_ring = false;
   size_t smem = 0;  // dynamic shared memory per CTA
   int nsl = 0;      // activation slots one CTA's units may touch
 };
@@ -889,17 +900,35 @@ BatchGeom batch_geom(const moe_cfg_t& c, int32_t T) {
   const long long nun_max = static_cast<long long>(T * k + (c.shared_inter > 0 ? 1 : 0)) * HB;
   const int upc = static_cast<int>((nun_max + b.G - 1) / b.G);  // units per CTA, at most
   b.nsl = upc > 0 ? (upc - 1) / HB + 2 : 0;
+  // [x rows][activation terms][ring], or, when that gains a ring stage,
+  // [activation terms][ring] with the x rows and then the logits in the
+  // ring's space until its first copy (a barrier before the first copy then
+  // keeps the x reads ahead of it)
+  const size_t xbytes = align_up(static_cast<size_t>(T) * b.xs, 128);
+  const size_t tbytes = align_up(static_cast<size_t>(b.nsl) * 2 * T * b.cs, 128);
+  {
+    const size_t bud = 227 * 1024 - kBtStaticSmem;
+    const size_t sep = xbytes + tbytes < bud ? (bud - xbytes - tbytes) / b.stage : 0;
+    const size_t ali = tbytes < bud ? (bud - tbytes) / b.stage : 0;
+    b.x_in_ring = std::min<size_t>(ali, kBtMaxStages) > std::min<size_t>(sep, kBtMaxStages);
+  }
   size_t off = 0;
-  b.off_xh = static_cast<uint32_t>(off);
-  off += align_up(static_cast<size_t>(T) * b.xs, 128);
+  if (!b.x_in_ring) {
+    b.off_xh = 0;
+    off += xbytes;
+  }
   b.off_terms = static_cast<uint32_t>(off);
   off += align_up(static_cast<size_t>(b.nsl) * 2 * T * b.cs, 128);
   b.off_ring = static_cast<uint32_t>(off);
+  if (b.x_in_ring) b.off_xh = b.off_ring;
+  b.off_lg = static_cast<uint32_t>(b.x_in_ring ? off + xbytes : off);
   const size_t budget = 227 * 1024 - kBtStaticSmem;
   const size_t ns = off < budget ? (budget - off) / b.stage : 0;
-  b.ns = static_cast<int>(ns > static_cast<size_t>(kBtMaxStages) ? kBtMaxStages : ns) & ~1;  // even
-  // the ring also holds phase 2's logits
-  const size_t ring = std::max(static_cast<size_t>(b.ns) * b.stage, static_cast<size_t>(T) * b.Lst * 4);
+  // an even count keeps every pass's gate and up stages adjacent (64 bytes
+  // apart modulo 128); an odd one costs 2-way conflicts on the wrapping pass
+  b.ns = static_cast<int>(ns > static_cast<size_t>(kBtMaxStages) ? kBtMaxStages : ns);
+  const size_t ring = std::max(static_cast<size_t>(b.ns) * b.stage,
+                               (b.x_in_ring ? xbytes : 0) + static_cast<size_t>(T) * b.Lst * 4);
   b.smem = off + ring;
   return b;
 }
@@ -971,7 +1000,8 @@ moe_status_t launch_decode_batch(const moe_cfg_t& c, const BlockPtrs& p, uint8_t
   a.Imax = b.Imax;
   a.xs = b.xs; a.cs = b.cs;
   a.gs13 = b.gs13; a.gs2 = b.gs2; a.stage = b.stage; a.ns = b.ns;
-  a.off_xh = b.off_xh; a.off_terms = b.off_terms; a.off_ring = b.off_ring;
+  a.off_terms = b.off_terms; a.off_ring = b.off_ring; a.off_xh = b.off_xh; a.off_lg = b.off_lg;
+  a.x_in_ring = b.x_in_ring ? 1 : 0;
   a.timeout_ns = wait_timeout_ns();
 #ifdef MOE_PHASE_TRACE
   a.trace = trace_next_record();
