@@ -100,11 +100,12 @@ typedef struct moe_cfg {
 } moe_cfg_t;
 
 /* cfg->flags bits selecting the T > 1 path (at most one of SIMT, TC and
- * SINGLE).  With none of them the library picks: for 2 <= T <= 8 the
- * single-launch kernel when the shape allows (E <= 256, top_k <= 8, H a
- * multiple of 256 up to 2048, I and Is multiples of 16), else the tcgen05
- * kernels when the shape allows (bf16, H % 128 == 0, I and Is multiples of
- * 64), else the CUDA-core kernels. */
+ * SINGLE).  With none of them the library picks: the single-launch kernel
+ * when the shape allows it (E <= 256, top_k <= 8, H a multiple of 256 up to
+ * 2048, I and Is multiples of 16) for 2 <= T <= 8, and for T <= 16 when the
+ * tcgen05 kernels are not available; else the tcgen05 kernels when the shape
+ * allows (bf16, H % 128 == 0, I and Is multiples of 64); else the CUDA-core
+ * kernels. */
 #define MOE_FLAG_GROUPED_SIMT 1  /* T > 1 on the CUDA-core grouped kernels      */
 #define MOE_FLAG_GROUPED_TC 2    /* T > 1 on the tcgen05 grouped kernels;
                                     MOE_ERR_UNSUPPORTED if the shape does not allow it */
@@ -121,7 +122,7 @@ typedef struct moe_cfg {
                                     sum, one rounding to out_dtype), so a stack
                                     of layers chains out -> x with no extra
                                     kernel.  Both the T = 1 and T > 1 paths. */
-#define MOE_FLAG_GROUPED_SINGLE 16 /* 2 <= T <= 8 in one launch: the T = 1
+#define MOE_FLAG_GROUPED_SINGLE 16 /* 2 <= T <= 16 in one launch: the T = 1
                                     kernel's design, the tokens as the
                                     tensor-core steps' B columns and the
                                     selected experts' union streamed once;

@@ -1,4 +1,4 @@
-// moe_batch.cu — the decode MoE block for 2 <= T <= 8 tokens in one launch.
+// moe_batch.cu — the decode MoE block for 2 <= T <= 16 tokens in one launch.
 //
 // What it computes: the block of the T = 1 kernel for each of T tokens
 // ("BI-V100 inference work log", Parts 3, 4, 9, 10): router GEMV, softmax and
@@ -57,7 +57,7 @@ namespace moe {
 constexpr int kBtThreads = 256;             // the 8 computing warps
 constexpr int kBtWarps = kBtThreads / 32;
 constexpr int kBtBlock = kBtThreads + 32;   // plus the warp that issues the ring's copies
-constexpr int kBtMaxPairs = 64;  // T * k <= kBatchMaxT * 8
+constexpr int kBtMaxPairs = kBatchMaxT * 8;  // T * k
 constexpr int kBtRows1 = 32;     // routing-independent rows per CTA (host-checked)
 constexpr int kBtMaxSlots = 4;   // activation slots one CTA's W2 units may touch (host-checked)
 constexpr int kBtMaxStages = 8;  // ring stages
@@ -174,13 +174,15 @@ struct TileGemv {
   }
 };
 
-// Lane (g, t) of a finished tile holds rows g / g + 8 of columns 2t, 2t + 1.
-__device__ __forceinline__ void store_tile(float (*part)[8], int row0, int lane, const float (&acc)[2][4]) {
+// Lane (g, t) of a finished tile holds rows g / g + 8 of columns 2t, 2t + 1
+// (columns c0 + 2t, c0 + 2t + 1 of part).
+template <int W>
+__device__ __forceinline__ void store_tile(float (*part)[W], int row0, int c0, int lane, const float (&acc)[2][4]) {
   const int g = lane >> 2, t = lane & 3;
-  part[row0 + g][2 * t] = acc[0][0] + acc[1][0];
-  part[row0 + g][2 * t + 1] = acc[0][1] + acc[1][1];
-  part[row0 + g + 8][2 * t] = acc[0][2] + acc[1][2];
-  part[row0 + g + 8][2 * t + 1] = acc[0][3] + acc[1][3];
+  part[row0 + g][c0 + 2 * t] = acc[0][0] + acc[1][0];
+  part[row0 + g][c0 + 2 * t + 1] = acc[0][1] + acc[1][1];
+  part[row0 + g + 8][c0 + 2 * t] = acc[0][2] + acc[1][2];
+  part[row0 + g + 8][c0 + 2 * t + 1] = acc[0][3] + acc[1][3];
 }
 
 // v ~ t0 + t1 in the storage type (t0 = rn(v), t1 = rn(v - t0)), packed
@@ -241,19 +243,23 @@ struct BatchArgs {
 #endif
 };
 
-template <int DT>
+// MAXT: the most tokens of the instantiation (8 or 16): the tokens are
+// MAXT / 8 B-column blocks of the weight GEMVs and the two activation terms
+// per token MAXT / 4 blocks of the down GEMV.
+template <int DT, int MAXT>
 __global__ void __launch_bounds__(kBtBlock, 1) decode_batch_kernel(const BatchArgs a) {
+  constexpr int NBT = MAXT / 8, NBC = MAXT / 4, MAXP = MAXT * 8;
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ float s_red[kBtWarps][kBtRows1][8];  // per-warp partial tiles (rows x tokens)
-  __shared__ int s_ids[kBatchMaxT][8];
-  __shared__ float s_sel[kBatchMaxT][8];
-  __shared__ float s_w[kBatchMaxT][8];
-  __shared__ float s_gate[kBatchMaxT];
-  __shared__ float s_uw[kBtMaxPairs][kBatchMaxT];  // routing weight of (union expert, token), 0 = not routed
-  __shared__ uint32_t s_utok[kBtMaxPairs];         // tokens routed to a union expert (bit t)
-  __shared__ int s_uexp[kBtMaxPairs];              // expert id of union slot u (ascending)
-  __shared__ int s_uslot[kBatchMaxT][8];           // union slot of (token, rank)
-  __shared__ float s_unsc[kBtMaxSlots][kBatchMaxT];  // fp16: the power of two undoing a row's term scale
+  __shared__ float s_red[kBtWarps][kBtRows1][MAXT];  // per-warp partial tiles (rows x tokens)
+  __shared__ int s_ids[MAXT][8];
+  __shared__ float s_sel[MAXT][8];
+  __shared__ float s_w[MAXT][8];
+  __shared__ float s_gate[MAXT];
+  __shared__ float s_uw[MAXP][MAXT];      // routing weight of (union expert, token), 0 = not routed
+  __shared__ uint32_t s_utok[MAXP];       // tokens routed to a union expert (bit t)
+  __shared__ int s_uexp[MAXP];            // expert id of union slot u (ascending)
+  __shared__ int s_uslot[MAXT][8];        // union slot of (token, rank)
+  __shared__ float s_unsc[kBtMaxSlots][MAXT];  // fp16: the power of two undoing a row's term scale
   __shared__ __align__(8) uint64_t s_full[kBtMaxStages];   // ring stage landed
   __shared__ __align__(8) uint64_t s_empty[kBtMaxStages];  // ring stage read by the 8 computing warps
   __shared__ int s_nU;
@@ -277,8 +283,8 @@ __global__ void __launch_bounds__(kBtBlock, 1) decode_batch_kernel(const BatchAr
   constexpr int LREP = kLogitReplicas;
 
   MOE_STAMP(0);  // entry
-  for (int i = tid; i < kBtMaxPairs * kBatchMaxT; i += kBtThreads) (&s_uw[0][0])[i] = 0.0f;
-  if (tid < kBtMaxPairs) s_utok[tid] = 0u;
+  for (int i = tid; i < MAXP * MAXT; i += kBtThreads) (&s_uw[0][0])[i] = 0.0f;
+  if (tid < MAXP) s_utok[tid] = 0u;
   if (tid == 0) {
     s_fail = 0;
     for (int st = 0; st < a.ns; ++st) {
@@ -456,15 +462,18 @@ __global__ void __launch_bounds__(kBtBlock, 1) decode_batch_kernel(const BatchAr
   MOE_STAMP(2);  // x staged
 
   for (int rg = 0; rg < R1; rg += 16) {
-    float acc[2][4] = {};
     if (rg > 0) {
       bool va, vb;
       const uint8_t* ra = p1_row(rg + g, va);
       const uint8_t* rb = p1_row(rg + 8 + g, vb);
       gv.load_global(ra, va, rb, vb, c0w, cendw, t4);
     }
-    gv.mma(xha, a.xs, T, c0w, cendw, lane, acc);
-    store_tile(s_red[warp], rg, lane, acc);
+#pragma unroll
+    for (int nb = 0; nb < NBT; ++nb) {  // tokens 8 nb .. 8 nb + 7
+      float acc[2][4] = {};
+      gv.mma(xha + nb * 8 * a.xs, a.xs, T - 8 * nb, c0w, cendw, lane, acc);
+      store_tile(s_red[warp], rg, 8 * nb, lane, acc);
+    }
   }
   cons_sync();
   MOE_STAMP(3);  // phase-1 dot products summed
@@ -496,23 +505,24 @@ __global__ void __launch_bounds__(kBtBlock, 1) decode_batch_kernel(const BatchAr
 
   MOE_STAMP(4);  // phase-1 results published
 
-  // ---- phase 2: per token, its logits, top-k and routing weights (warp t)
-  if (warp < T) {
-    float* lw = lg + warp * a.Lst;
-    const uint64_t* src = a.ll_logits + static_cast<size_t>(cta % LREP) * a.lrep + static_cast<size_t>(warp) * a.Lst;
+  // ---- phase 2: per token, its logits, top-k and routing weights (warp t
+  // takes tokens t, t + 8)
+  for (int tw = warp; tw < T; tw += kBtWarps) {
+    float* lw = lg + tw * a.Lst;
+    const uint64_t* src = a.ll_logits + static_cast<size_t>(cta % LREP) * a.lrep + static_cast<size_t>(tw) * a.Lst;
     const bool ok = __all_sync(0xffffffffu, ll_gather<8>(src, lw, E1, lane, 32, epoch, global_ns() + a.timeout_ns));
     MOE_STAMP(5);  // logits gathered (warp 0)
     if (!ok) {
       if (lane == 0) s_fail = kDevTimeoutLogits;
     } else {
-      warp_topk_sorted8(lw, E, k, s_ids[warp], s_sel[warp]);
+      warp_topk_sorted8(lw, E, k, s_ids[tw], s_sel[tw]);
       MOE_STAMP(15);  // warp 0's top-k done
-      warp_routing_weights(lw, E, s_sel[warp], k, a.norm_topk, s_w[warp]);
-      if (lane == 0) s_gate[warp] = a.has_gate ? sigmoid_f(lw[E]) : 1.0f;
+      warp_routing_weights(lw, E, s_sel[tw], k, a.norm_topk, s_w[tw]);
+      if (lane == 0) s_gate[tw] = a.has_gate ? sigmoid_f(lw[E]) : 1.0f;
       __syncwarp();
       if (cta == 0 && lane < k) {
-        a.topk_ids[warp * k + lane] = s_ids[warp][lane];
-        a.topk_w[warp * k + lane] = s_w[warp][lane];
+        a.topk_ids[tw * k + lane] = s_ids[tw][lane];
+        a.topk_w[tw * k + lane] = s_w[tw][lane];
       }
     }
   }
@@ -530,17 +540,24 @@ __global__ void __launch_bounds__(kBtBlock, 1) decode_batch_kernel(const BatchAr
   }
   if (ranked && warp == 0) {
     // the union U of selected experts (ascending id) and, per (token, rank),
-    // its slot in U: lane l takes selections l and l + 32; lane w < 8 keeps
-    // word w of the 256-bit selection mask (no arrays: they would go to
-    // local memory)
-    const int q0 = lane, q1 = lane + 32;
-    const int e0 = q0 < T * k ? s_ids[q0 / k][q0 % k] : -1;
-    const int e1 = q1 < T * k ? s_ids[q1 / k][q1 % k] : -1;
+    // its slot in U: lane l takes selections l, l + 32, ...; lane w < 8
+    // keeps word w of the 256-bit selection mask (every loop is unrolled, so
+    // nothing is indexed at run time: that would put the arrays in local
+    // memory)
+    constexpr int NSEL = MAXP / 32;
+    int esel[NSEL];
+#pragma unroll
+    for (int h = 0; h < NSEL; ++h) {
+      const int q = lane + 32 * h;
+      esel[h] = q < T * k ? s_ids[q / k][q % k] : -1;
+    }
     uint32_t word = 0;
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
-      const uint32_t m = __reduce_or_sync(0xffffffffu, (e0 >= 0 && (e0 >> 5) == w ? 1u << (e0 & 31) : 0u) |
-                                                           (e1 >= 0 && (e1 >> 5) == w ? 1u << (e1 & 31) : 0u));
+      uint32_t mine = 0;
+#pragma unroll
+      for (int h = 0; h < NSEL; ++h) mine |= esel[h] >= 0 && (esel[h] >> 5) == w ? 1u << (esel[h] & 31) : 0u;
+      const uint32_t m = __reduce_or_sync(0xffffffffu, mine);
       if (lane == w) word = m;
     }
     const int cnt = __popc(word);
@@ -551,7 +568,9 @@ __global__ void __launch_bounds__(kBtBlock, 1) decode_batch_kernel(const BatchAr
       if (lane >= o) incl += v;
     }
     const int excl = incl - cnt;
-    auto place = [&](int q, int e) {
+#pragma unroll
+    for (int h = 0; h < NSEL; ++h) {
+      const int q = lane + 32 * h, e = esel[h];
       const uint32_t mwd = __shfl_sync(0xffffffffu, word, max(e, 0) >> 5);
       const int base = __shfl_sync(0xffffffffu, excl, max(e, 0) >> 5);
       if (e >= 0) {
@@ -561,9 +580,7 @@ __global__ void __launch_bounds__(kBtBlock, 1) decode_batch_kernel(const BatchAr
         s_uw[u][tk] = s_w[tk][j];
         atomicOr(&s_utok[u], 1u << tk);
       }
-    };
-    place(q0, e0);
-    place(q1, e1);
+    }
     if (lane < 8) {
       int r = excl;
       for (uint32_t mm = word; mm; mm &= mm - 1u) s_uexp[r++] = lane * 32 + __ffs(mm) - 1;
@@ -582,16 +599,19 @@ __global__ void __launch_bounds__(kBtBlock, 1) decode_batch_kernel(const BatchAr
   // x's B fragments for this warp's 16-column steps of phase 3 (column n =
   // token g, rows k = 2t, 2t + 1 and 2t + 8, 2t + 9 of the step), read before
   // the ring's first copy overwrites the x rows
-  uint32_t bx[16][2];
+  uint32_t bx[NBT][16][2];
   auto load_bx = [&]() {
 #pragma unroll
-    for (int kk = 0; kk < 16; ++kk) {
-      const bool in = npass > 0 && kk < kpw && g < T;
-      const int k0 = (warp * kpw + kk) * 16 + 2 * t4;
-      const uint32_t xa = xha + static_cast<uint32_t>(in ? g : 0) * a.xs + 2 * (in ? k0 : 0);
-      bx[kk][0] = in ? lds32(xa) : 0u;
-      bx[kk][1] = in ? lds32(xa + 16) : 0u;
-    }
+    for (int nb = 0; nb < NBT; ++nb)
+#pragma unroll
+      for (int kk = 0; kk < 16; ++kk) {
+        const int tk = 8 * nb + g;
+        const bool in = npass > 0 && kk < kpw && tk < T;
+        const int k0 = (warp * kpw + kk) * 16 + 2 * t4;
+        const uint32_t xa = xha + static_cast<uint32_t>(in ? tk : 0) * a.xs + 2 * (in ? k0 : 0);
+        bx[nb][kk][0] = in ? lds32(xa) : 0u;
+        bx[nb][kk][1] = in ? lds32(xa + 16) : 0u;
+      }
   };
   load_bx();
   if (a.x_in_ring) {
@@ -636,7 +656,7 @@ __global__ void __launch_bounds__(kBtBlock, 1) decode_batch_kernel(const BatchAr
   const uint32_t lm13 = static_cast<uint32_t>(lane & 3) * a.gs13 + ((lane >> 3) & 1) * rb13 + (lane >> 4) * 16;
   if (npass > 0) {
     for (int q = 0; q < npass; ++q) {
-      float acc[2][4] = {};
+      float acc[NBT][2][4] = {};
       wait_item(2 * q);
       wait_item(2 * q + 1);
       const uint32_t sa = ring_a + ((2 * q + ((lane >> 2) & 1)) % a.ns) * stage_bytes + lm13 +
@@ -646,11 +666,14 @@ __global__ void __launch_bounds__(kBtBlock, 1) decode_batch_kernel(const BatchAr
         if (kk < kpw) {
           uint32_t a0, a1, a2, a3;
           ldsm_x4(sa + kk * 32, a0, a1, a2, a3);
-          mma16816<DT>(acc[kk & 1], a0, a1, a2, a3, bx[kk][0], bx[kk][1]);
+#pragma unroll
+          for (int nb = 0; nb < NBT; ++nb)
+            mma16816<DT>(acc[nb][kk & 1], a0, a1, a2, a3, bx[nb][kk][0], bx[nb][kk][1]);
         }
       release_item(2 * q, 1);
       release_item(2 * q + 1, 1);
-      store_tile(s_red[warp], (q & 1) * 16, lane, acc);
+#pragma unroll
+      for (int nb = 0; nb < NBT; ++nb) store_tile(s_red[warp], (q & 1) * 16, 8 * nb, lane, acc[nb]);
       if (q == 0) MOE_STAMP(12);  // thread 0: first pass's dot products done
       cons_sync();  // this pass's partials are visible
       if (q == 1) MOE_STAMP(13);  // second pass done (all warps)
@@ -762,28 +785,31 @@ __global__ void __launch_bounds__(kBtBlock, 1) decode_batch_kernel(const BatchAr
       const uint32_t sa = ring_a + ((n13 + m) % a.ns) * stage_bytes + v * unit_bytes +
                           static_cast<uint32_t>(lane & 7) * a.gs2 + ((lane >> 3) & 1) * Iu * 2 + (lane >> 4) * 16;
       const uint32_t bb = terms_a + ls * slot_bytes + static_cast<uint32_t>(g) * a.cs + 4 * t4;
-      const bool b0v = g < 2 * T, b1v = g + 8 < 2 * T;
-      float acc0[2][4] = {}, acc1[2][4] = {};  // B columns 0-7 (tokens 0-3), 8-15 (tokens 4-7)
+      // B column block nc holds columns 8 nc .. 8 nc + 7 (tokens 4 nc .. 4 nc + 3)
+      float acc[NBC][2][4] = {};
       // NK 16-column steps at a time: every operand load issued before the
       // tensor-core steps, two accumulator chains (static indices: a runtime
       // index would put the accumulators in local memory)
       auto ksteps = [&](auto nk_c, int ks) {
         constexpr int NK = decltype(nk_c)::value;
-        uint32_t av[NK][4], xv[NK][2], yv[NK][2];
+        uint32_t av[NK][4], xv[NK][NBC][2];
 #pragma unroll
         for (int i = 0; i < NK; ++i) {
           ldsm_x4(sa + (ks + i) * 32, av[i][0], av[i][1], av[i][2], av[i][3]);
           const uint32_t ba = bb + (ks + i) * 32;
-          xv[i][0] = b0v ? lds32(ba) : 0u;
-          xv[i][1] = b0v ? lds32(ba + 16) : 0u;
-          yv[i][0] = T > 4 && b1v ? lds32(ba + 8 * a.cs) : 0u;
-          yv[i][1] = T > 4 && b1v ? lds32(ba + 8 * a.cs + 16) : 0u;
+#pragma unroll
+          for (int nc = 0; nc < NBC; ++nc) {
+            const bool bv = 8 * nc + g < 2 * T;
+            xv[i][nc][0] = bv ? lds32(ba + 8 * nc * a.cs) : 0u;
+            xv[i][nc][1] = bv ? lds32(ba + 8 * nc * a.cs + 16) : 0u;
+          }
         }
 #pragma unroll
-        for (int i = 0; i < NK; ++i) {
-          mma16816<DT>(acc0[i & 1], av[i][0], av[i][1], av[i][2], av[i][3], xv[i][0], xv[i][1]);
-          if (T > 4) mma16816<DT>(acc1[i & 1], av[i][0], av[i][1], av[i][2], av[i][3], yv[i][0], yv[i][1]);
-        }
+        for (int i = 0; i < NK; ++i)
+#pragma unroll
+          for (int nc = 0; nc < NBC; ++nc)
+            if (8 * nc < 2 * T)
+              mma16816<DT>(acc[nc][i & 1], av[i][0], av[i][1], av[i][2], av[i][3], xv[i][nc][0], xv[i][nc][1]);
       };
       const int nks = Iu >> 4;
       int ks = 0;
@@ -791,8 +817,8 @@ __global__ void __launch_bounds__(kBtBlock, 1) decode_batch_kernel(const BatchAr
       for (; ks < nks; ++ks) ksteps(std::integral_constant<int, 1>{}, ks);
       release_item(n13 + m, kBtWarps / 2);
       if (us == 0) MOE_STAMP(19);  // warp 0's first unit computed
-      // lane (g, t4): tile rows g, g + 8 (unit rows 2g, 2g + 1) of token t4
-      // (columns hi, lo) and 4 + t4
+      // lane (g, t4): tile rows g, g + 8 (unit rows 2g, 2g + 1) of tokens
+      // 4 nc + t4 (columns hi, lo of block nc)
       auto publish = [&](int tk, const float(&ac)[2][4]) {
         if (tk < T && (sh || ((s_utok[s] >> tk) & 1u))) {
           float unsc = 1.0f;
@@ -804,8 +830,8 @@ __global__ void __launch_bounds__(kBtBlock, 1) decode_batch_kernel(const BatchAr
           ll_store(pr + 2 * g + 1, y1, epoch);
         }
       };
-      publish(t4, acc0);
-      publish(4 + t4, acc1);
+#pragma unroll
+      for (int nc = 0; nc < NBC; ++nc) publish(4 * nc + t4, acc[nc]);
     } else {
       release_item(n13 + m, kBtWarps / 2);
     }
@@ -876,9 +902,10 @@ struct BatchGeom {
   int nsl = 0;      // activation slots one CTA's units may touch
 };
 
-// Static shared memory of decode_batch_kernel (the arrays declared in it),
-// rounded up; the dynamic part gets the rest of the 227 KB.
-constexpr size_t kBtStaticSmem = 16 * 1024;
+// Static shared memory of decode_batch_kernel (the arrays declared in it,
+// for at most 8 and at most 16 tokens), rounded up; the dynamic part gets the
+// rest of the 227 KB.
+static size_t bt_static_smem(int32_t T) { return T <= 8 ? 16 * 1024 : 32 * 1024; }
 
 BatchGeom batch_geom(const moe_cfg_t& c, int32_t T) {
   BatchGeom b;
@@ -907,7 +934,7 @@ BatchGeom batch_geom(const moe_cfg_t& c, int32_t T) {
   const size_t xbytes = align_up(static_cast<size_t>(T) * b.xs, 128);
   const size_t tbytes = align_up(static_cast<size_t>(b.nsl) * 2 * T * b.cs, 128);
   {
-    const size_t bud = 227 * 1024 - kBtStaticSmem;
+    const size_t bud = 227 * 1024 - bt_static_smem(T);
     const size_t sep = xbytes + tbytes < bud ? (bud - xbytes - tbytes) / b.stage : 0;
     const size_t ali = tbytes < bud ? (bud - tbytes) / b.stage : 0;
     b.x_in_ring = std::min<size_t>(ali, kBtMaxStages) > std::min<size_t>(sep, kBtMaxStages);
@@ -922,7 +949,7 @@ BatchGeom batch_geom(const moe_cfg_t& c, int32_t T) {
   b.off_ring = static_cast<uint32_t>(off);
   if (b.x_in_ring) b.off_xh = b.off_ring;
   b.off_lg = static_cast<uint32_t>(b.x_in_ring ? off + xbytes : off);
-  const size_t budget = 227 * 1024 - kBtStaticSmem;
+  const size_t budget = 227 * 1024 - bt_static_smem(T);
   const size_t ns = off < budget ? (budget - off) / b.stage : 0;
   // an even count keeps every pass's gate and up stages adjacent (64 bytes
   // apart modulo 128); an odd one costs 2-way conflicts on the wrapping pass
@@ -950,7 +977,6 @@ bool batch_shape_ok(const moe_cfg_t& c, int32_t T) {
   if (b.G < 1 || b.G > E1 || b.G > kBtMaxCtas) return false;  // every CTA owns a logit row
   if (2 * ((E1 + Is + b.G - 1) / b.G) > kBtRows1) return false;
   if (b.nsl > kBtMaxSlots) return false;
-  if (b.nsl * T * b.Imax > 2 * 16 * kBtThreads) return false;  // activation gather: 16 word pairs per thread
   return b.ns >= 2;
 }
 
@@ -971,7 +997,7 @@ size_t batch_ws_words(const moe_cfg_t& c, int32_t T, size_t& logit_words, size_t
 moe_status_t launch_decode_batch(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws, const WsLayout& L,
                                  int32_t T, cudaStream_t st) {
   if (!batch_shape_ok(c, T) || !L.bt_logits)
-    return set_error(MOE_ERR_UNSUPPORTED, "single-launch batch path: needs 2 <= T <= 8, E <= 256, k <= 8, "
+    return set_error(MOE_ERR_UNSUPPORTED, "single-launch batch path: needs 2 <= T <= 16, E <= 256, k <= 8, "
                                           "H a multiple of 256 up to 2048, I and Is multiples of 16");
   const BatchGeom b = batch_geom(c, T);
   BatchArgs a;
@@ -1025,8 +1051,12 @@ moe_status_t launch_decode_batch(const moe_cfg_t& c, const BlockPtrs& p, uint8_t
     stat_kernels(1);
     return MOE_OK;
   };
-  if (c.dtype == MOE_BF16) return launch(decode_batch_kernel<MOE_BF16>);
-  return launch(decode_batch_kernel<MOE_F16>);
+  if (T <= 8) {
+    if (c.dtype == MOE_BF16) return launch(decode_batch_kernel<MOE_BF16, 8>);
+    return launch(decode_batch_kernel<MOE_F16, 8>);
+  }
+  if (c.dtype == MOE_BF16) return launch(decode_batch_kernel<MOE_BF16, 16>);
+  return launch(decode_batch_kernel<MOE_F16, 16>);
 }
 
 }  // namespace moe

@@ -21,7 +21,7 @@ constexpr int kLogitReplicas = 16;
 constexpr int kActReplicas = 8;
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 // Most tokens of the single-launch batch kernel (2 <= T <= kBatchMaxT).
-constexpr int kBatchMaxT = 8;
+constexpr int kBatchMaxT = 16;
 
 // Byte offsets of every region of one workspace, for `T` tokens of a cfg.
 struct WsLayout {

@@ -174,9 +174,9 @@ def test_single_launch_batch_workspace(m):
         grouped_only = m.moe_workspace_bytes(m.MoeCfg(4096, 256, 8, 512, 512, m.MOE_BF16, has_shared_gate=1), T)
         assert m.moe_workspace_bytes(c, T) >= words * 8
         assert grouped_only > 0  # H = 4096: no batch regions, still a valid T > 1 workspace
-    # the 8-token partial rows alone (65 slots x 8 tokens x 2048 words) outweigh
-    # everything a 9-token workspace holds
-    assert m.moe_workspace_bytes(c, 8) > m.moe_workspace_bytes(c, 9)
+    # the 16-token partial rows alone (129 slots x 16 tokens x 2048 words)
+    # outweigh everything a 17-token workspace holds
+    assert m.moe_workspace_bytes(c, 16) > m.moe_workspace_bytes(c, 17)
 
 
 def test_tensor_core_path_workspace_is_laid_out_for_bf16_shapes(m):

@@ -243,12 +243,12 @@ def test_no_renormalisation_no_shared_expert(m, flags):
 
 
 def test_fp16_batches_take_the_cuda_core_path(m):
-    """fp16 with T > 8 runs the CUDA-core grouped kernels by default (the
-    tensor-core passes are bf16 only; up to 8 tokens take the single-launch
+    """fp16 with T > 16 runs the CUDA-core grouped kernels by default (the
+    tensor-core passes are bf16 only; up to 16 tokens take the single-launch
     kernel) and matches the oracle on every token, as does an fp16 batch of 6
     on the CUDA-core kernels."""
     wl = moe_synth.workload("sharded_decode")
-    T = 12
+    T = 20
     g = moe_synth.make_layer(wl, 3, T, device=DEV)
     m.moe_reset_stats()
     ids, w, out = _grouped(m, wl, g, T)
