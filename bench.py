@@ -499,11 +499,14 @@ def grouped_flops(wl, T):
     return 2 * T * (E * H + k * 3 * I * H + 3 * Is * H)
 
 
-def grouped_stack(m, wl, T, layers, dev, steps, warmup, repeats, xs=None):
+GROUPED_PATH_FLAGS = {"auto": 0, "simt": 1, "tc": 2, "single": 16}  # MOE_FLAG_GROUPED_* bits
+
+
+def grouped_stack(m, wl, T, layers, dev, steps, warmup, repeats, xs=None, flags=0):
     """Time one grouped forward of T tokens through every layer (a CUDA graph
     of len(layers) calls); returns (median ms per step, kernels per layer,
     path, mean distinct experts per layer)."""
-    cfg = m.cfg_from_workload(wl)
+    cfg = m.cfg_from_workload(wl, None, flags)
     L, H, k = len(layers), wl.hidden, wl.top_k
     xs = xs or [moe_synth.make_x(wl, l, T, dev) for l in range(L)]
     outs = torch.empty(L, T, H, dtype=cfg.out_torch_dtype, device=dev)
@@ -631,7 +634,8 @@ def run_grouped(args, wl, ws_n, rank, local):
     barrier(ws_n)
     clocks.start()
     time.sleep(0.3)
-    med, kpl, path, distinct = grouped_stack(m, wl, T, layers, dev, K, W, args.repeats or 5, xs=xs)
+    med, kpl, path, distinct = grouped_stack(m, wl, T, layers, dev, K, W, args.repeats or 5, xs=xs,
+                                             flags=GROUPED_PATH_FLAGS[args.grouped_path])
     clk = clocks.stop()
     ms_max = reduce_max(med, ws_n)
     if rank != 0:
@@ -683,6 +687,8 @@ def main():
     ap.add_argument("--repeats", type=int, default=0,
                     help="timed regions of K steps, the median reported (0: at least 5, about 1 s in all)")
     ap.add_argument("--no-workloads", action="store_true", help="headline workload only")
+    ap.add_argument("--grouped-path", default="auto", choices=sorted(GROUPED_PATH_FLAGS),
+                    help="T > 1 path of --workload small_batch / chunked_prefill (auto: the library's choice)")
     ap.add_argument("--no-static-weights", action="store_true",
                     help="T=1: do not let layer kernels read weights before the previous layer completes")
     args = ap.parse_args()
