@@ -158,14 +158,14 @@ __device__ __forceinline__ bool epi_any(bool v) {
 // with double buffering).  The token operand is the gathered rows Xs (rows
 // pos0.. of the tile's pairs), or with DIRECT (T <= 16) x itself: every tile
 // then computes all T token columns and pair j of the tile takes the column of
-// its token.
+// its token.  Tiles are taken dynamically as in the W2 pass below.
 template <int DT, int N, int MT, bool DIRECT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_w13_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapAs,
                   const __grid_constant__ CUtensorMap mapB, const TcTile* tiles,
                   const int32_t* n_tiles_p, int H, int I, int Is, int E, int act_stride,
                   uint16_t* __restrict__ act_hi, uint16_t* __restrict__ act_lo, Control* ctrl, uint64_t timeout,
-                  const int32_t* perm, int direct_T, int k) {
+                  const int32_t* perm, int direct_T, int k, int32_t* tile_ctr) {
   pdl_launch_dependents();  // let the next kernel on the stream launch early
   constexpr uint32_t kStage = MT * kTileA + N * 128;
   constexpr int kStg = 128 * 17 * 4;
@@ -174,7 +174,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* stg = reinterpret_cast<float*>(smem + kStages * kStage);  // [128][17] epilogue staging
-  __shared__ __align__(8) uint64_t full[kStages], empty[kStages], tfull[2], tempty[2], done;
+  __shared__ __align__(8) uint64_t full[kStages], empty[kStages], tfull[2], tempty[2], done, tq_full[4], tq_empty[4];
+  __shared__ int s_tq[4];  // tile queue: the producer's tiles, in order, for the MMA and epilogue warps
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int s_abort;
   __shared__ int s_tok[DIRECT ? N : 1];  // DIRECT: token of each pair of the current tile
@@ -183,6 +184,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
     for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], 4); }
+    for (int a = 0; a < 4; ++a) { mbar_init(&tq_full[a], 1); mbar_init(&tq_empty[a], 2); }
     mbar_init(&done, 1);
     mbar_fence_init();
     s_abort = 0;
@@ -209,7 +211,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued_mask = 0, issued_phase = 0;
-      for (int t = blockIdx.x; t < ntiles && !s_abort; t += gridDim.x) {
+      for (int j = 0; !s_abort; ++j) {
+        const int qs = j & 3;
+        if (j >= 4 && !tc_wait(&tq_empty[qs], ((j >> 2) - 1) & 1, timeout, &s_abort)) {
+          s_abort = 1;
+          report_error(ctrl, kDevTimeoutCopy, blockIdx.x);
+          break;
+        }
+        int t = j == 0 ? static_cast<int>(blockIdx.x) : static_cast<int>(gridDim.x) + atomicAdd(tile_ctr, 1);
+        if (t >= ntiles) t = -1;
+        s_tq[qs] = t;
+        mbar_arrive(&tq_full[qs]);
+        if (t < 0) break;
         const TcTile tl = tiles[t];
         const bool sh = tl.e == E;
         const CUtensorMap* mA = sh ? &mapAs : &mapA;
@@ -245,8 +258,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       constexpr uint32_t idesc = idesc_f16<DT, N>();
       int stage = 0;
       uint32_t phase = 0;
-      int it = 0;
-      for (int t = blockIdx.x; t < ntiles && !s_abort; t += gridDim.x, ++it) {
+      for (int it = 0; !s_abort; ++it) {
+        const int qs = it & 3;
+        if (!tc_wait(&tq_full[qs], (it >> 2) & 1, timeout, &s_abort)) {
+          s_abort = 1;
+          report_error(ctrl, kDevTimeoutCopy, blockIdx.x);
+          break;
+        }
+        const int t = s_tq[qs];
+        mbar_arrive(&tq_empty[qs]);
+        if (t < 0) break;
         const TcTile tl = tiles[t];
         const int ie = tl.e == E ? Is : I;
         const int nv = min(MT, ie / 64 - tl.m * MT);
@@ -291,8 +312,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int row = 32 * q + lane;          // TMEM lane this thread reads
     const int etid = threadIdx.x - 64;      // 0..127
     const int ar = etid & 63, half = etid >> 6;  // activation row and column half it computes
-    int it = 0;
-    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+    for (int it = 0;; ++it) {
+      const int qs = it & 3;
+      const bool okq = !s_abort && tc_wait(&tq_full[qs], (it >> 2) & 1, timeout, &s_abort);
+      const int t = okq ? s_tq[qs] : -1;
+      if (epi_any(!okq)) {  // every epilogue thread has read the queue entry
+        s_abort = 1;
+        report_error(ctrl, kDevTimeoutCopy, blockIdx.x);
+        break;
+      }
+      if (etid == 0) mbar_arrive(&tq_empty[qs]);
+      if (t < 0) break;
       const TcTile tl = tiles[t];
       const int ie = tl.e == E ? Is : I;
       const int nv = min(MT, ie / 64 - tl.m * MT);
@@ -357,7 +387,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 // =========================================================== W2 pass
 // MT 128-row M-tiles of W2 (output rows h) of one expert share every
-// activation (hi, lo) stage.
+// activation (hi, lo) stage.  Tiles are taken dynamically: CTA c starts with
+// tile c, then the producer takes the next from a global counter (SMs that
+// finish early take more) and passes each tile to the MMA and epilogue warps
+// through a 4-entry shared-memory queue (tq_full / tq_empty).
 template <int DT, int N, int MT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_w2_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapAs,
@@ -366,14 +399,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                  const TcTile* tiles, const int32_t* n_tiles_p,
                  const int32_t* perm, const float* topk_w,
                  const float* gate_logits, int gate_stride, int has_gate, int T, int H, int I, int Is,
-                 int E, int k, float* __restrict__ y, Control* ctrl, uint64_t timeout) {
+                 int E, int k, float* __restrict__ y, int32_t* tile_ctr, Control* ctrl, uint64_t timeout) {
   pdl_launch_dependents();  // let the next kernel on the stream launch early
   constexpr uint32_t kStage = MT * kTileA + 2 * N * 128;
   constexpr int kStages = kSmemBudget / kStage > 8 ? 8 : kSmemBudget / kStage;
   constexpr uint32_t kCols = 2 * MT * N;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t full[kStages], empty[kStages], tfull[2], tempty[2], done;
+  __shared__ __align__(8) uint64_t full[kStages], empty[kStages], tfull[2], tempty[2], done, tq_full[4], tq_empty[4];
+  __shared__ int s_tq[4];
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int s_abort;
   __shared__ int s_pair[N];
@@ -383,6 +417,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
     for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], 4); }
+    for (int a = 0; a < 4; ++a) { mbar_init(&tq_full[a], 1); mbar_init(&tq_empty[a], 2); }
     mbar_init(&done, 1);
     mbar_fence_init();
     s_abort = 0;
@@ -412,7 +447,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued_mask = 0, issued_phase = 0;
-      for (int t = blockIdx.x; t < ntiles && !s_abort; t += gridDim.x) {
+      for (int j = 0; !s_abort; ++j) {
+        const int qs = j & 3;
+        if (j >= 4 && !tc_wait(&tq_empty[qs], ((j >> 2) - 1) & 1, timeout, &s_abort)) {
+          s_abort = 1;
+          report_error(ctrl, kDevTimeoutCopy, blockIdx.x);
+          break;
+        }
+        int t = j == 0 ? static_cast<int>(blockIdx.x) : static_cast<int>(gridDim.x) + atomicAdd(tile_ctr, 1);
+        if (t >= ntiles) t = -1;
+        s_tq[qs] = t;
+        mbar_arrive(&tq_full[qs]);
+        if (t < 0) break;
         const TcTile tl = tiles[t];
         const bool sh = tl.e == E;
         const CUtensorMap* mA = sh ? &mapAs : &mapA;
@@ -447,8 +493,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       constexpr uint32_t idesc = idesc_f16<DT, N>();
       int stage = 0;
       uint32_t phase = 0;
-      int it = 0;
-      for (int t = blockIdx.x; t < ntiles && !s_abort; t += gridDim.x, ++it) {
+      for (int it = 0; !s_abort; ++it) {
+        const int qs = it & 3;
+        if (!tc_wait(&tq_full[qs], (it >> 2) & 1, timeout, &s_abort)) {
+          s_abort = 1;
+          report_error(ctrl, kDevTimeoutCopy, blockIdx.x);
+          break;
+        }
+        const int t = s_tq[qs];
+        mbar_arrive(&tq_empty[qs]);
+        if (t < 0) break;
         const TcTile tl = tiles[t];
         const int KB = (tl.e == E ? Is : I) / kBK;
         const int nv = min(MT, mtiles - tl.m * MT);
@@ -494,12 +548,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int q = warp & 3;
     const int row = 32 * q + lane;
     const int etid = threadIdx.x - 64;  // 0..127
-    int it = 0;
-    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+    for (int it = 0;; ++it) {
+      const int qs = it & 3;
+      const bool okq = !s_abort && tc_wait(&tq_full[qs], (it >> 2) & 1, timeout, &s_abort);
+      const int t = okq ? s_tq[qs] : -1;
+      // every epilogue thread has read the queue entry (and the previous
+      // tile's readers of s_pair / s_wt are done)
+      if (epi_any(!okq)) {
+        s_abort = 1;
+        report_error(ctrl, kDevTimeoutCopy, blockIdx.x);
+        break;
+      }
+      if (etid == 0) mbar_arrive(&tq_empty[qs]);
+      if (t < 0) break;
       const TcTile tl = tiles[t];
       const int nv = min(MT, mtiles - tl.m * MT);
       const int acc = it & 1;
-      if (epi_any(s_abort != 0)) break;  // also: previous tile's readers of s_pair / s_wt are done
       for (int c = etid; c < tl.n; c += 128) {
         const int p = perm[tl.pos0 + c];
         s_pair[c] = p;
@@ -944,7 +1008,7 @@ static moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uin
   auto launch13 = [&](auto kernel, size_t s13) {
     cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s13));
     launch_pdl(kernel, dim3(g13 > 0 ? g13 : 1), dim3(kTcThreads), s13, st, mA, mAs, mB, t13, sched, H, I, Is, E,
-               Imax, ahi, alo, ctrl, timeout, perm, direct ? T : 0, k);
+               Imax, ahi, alo, ctrl, timeout, perm, direct ? T : 0, k, sched + 2);
   };
   if (mt13 == 1) {
     if (direct) launch13(tc_w13_kernel<DT, N, 1, true>, tc_smem13<N, 1>());
@@ -957,7 +1021,8 @@ static moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uin
   auto launch2 = [&](auto kernel, size_t s2) {
     cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s2));
     launch_pdl(kernel, dim3(g2 > 0 ? g2 : 1), dim3(kTcThreads), s2, st, mW2, mW2s, mHi, mLo, mHiS, mLoS, t2,
-               sched + 1, perm, p.topk_w, glog, gate_stride, c.has_shared_gate, T, H, I, Is, E, k, y, ctrl, timeout);
+               sched + 1, perm, p.topk_w, glog, gate_stride, c.has_shared_gate, T, H, I, Is, E, k, y, sched + 3, ctrl,
+               timeout);
   };
   if (mt2 == 1) launch2(tc_w2_kernel<DT, N, 1>, tc_smem2<N, 1>());
   else launch2(tc_w2_kernel<DT, N, kMT>, tc_smem2<N, kMT>());

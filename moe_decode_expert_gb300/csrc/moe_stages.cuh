@@ -95,7 +95,6 @@ __device__ __forceinline__ void group_stage(const int32_t* ids, int T, int k, in
   __shared__ int32_t cnt[1025 + 1];
   __shared__ int32_t cur[1025 + 1];
   __shared__ int32_t tcnt[1025 + 1];
-  __shared__ int32_t wsum[32];
   const int tid = threadIdx.x;
   const int n = E + 1;  // experts + the shared expert
   for (int e = tid; e < n; e += 1024) cnt[e] = 0;
@@ -147,7 +146,6 @@ __device__ __forceinline__ void group_stage(const int32_t* ids, int T, int k, in
   if (e0 < n) { cur[e0] = pb; tcnt[e0] = tb; }
   if (e1 < n) { cur[e1] = pb + c0; tcnt[e1] = tb + t0; }
   __syncthreads();
-  (void)wsum;
   for (int e = tid; e < n; e += 1024) {
     offsets[e] = cur[e];
     counts_out[e] = cnt[e];
@@ -235,7 +233,12 @@ __device__ __forceinline__ void schedule_stage(const int32_t* counts,
   if (2 * tid + 1 < n) { pre13[2 * tid + 1] = b13 + a13[0]; pre2[2 * tid + 1] = b2 + a2[0]; }
   __syncthreads();
   const int tot13 = static_cast<int>(wtot[31] >> 32), tot2 = static_cast<int>(wtot[31] & 0xffffffffu);
-  if (tid == 0) { *n13 = tot13; *n2 = tot2; }
+  if (tid == 0) {
+    *n13 = tot13;
+    *n2 = tot2;
+    n13[2] = 0;  // the two passes' dynamic tile counters (n13[0..3] is the schedule block)
+    n13[3] = 0;
+  }
   // Fill both lists in parallel: tile i belongs to the last expert whose first
   // tile index is <= i (experts without tiles share their successor's start).
   for (int i = tid; i < tot13 + tot2; i += 1024) {
@@ -380,6 +383,8 @@ __device__ __forceinline__ void small_group_schedule(const int32_t* flat_ids, in
       sc.tot2 = i2;
       *n13 = i13;
       *n2 = i2;
+      n13[2] = 0;  // the two passes' dynamic tile counters
+      n13[3] = 0;
     }
   }
   __syncthreads();
