@@ -91,6 +91,22 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+// The same load without its wait: a load goes out while earlier values are
+// used; tmem_ld_wait() then tmem_ld_tie() on the destination before its first
+// use (the tie keeps the compiler from reading the registers above the wait).
+__device__ __forceinline__ void tmem_ld16_issue(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_ld_tie(uint32_t (&r)[16]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
+}
 __device__ __forceinline__ void named_bar_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
@@ -342,12 +358,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int mt = 0; mt < nv; ++mt) {
         const int i = (tl.m * MT + mt) * 64 + ar;
         const int ncols = DIRECT ? direct_T : tl.n;  // accumulator columns holding results
-        for (int c0 = 0; c0 < ncols; c0 += 16) {
-          float v[16];
-          tmem_ld16(tbase + (static_cast<uint32_t>(32 * q) << 16) +
-                        static_cast<uint32_t>((acc * MT + mt) * N + c0), v);
+        const uint32_t ta = tbase + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>((acc * MT + mt) * N);
+        // 16 columns at a time through the staging rows; the next block's TMEM
+        // load is in flight meanwhile (two register blocks in turn)
+        auto block = [&](const uint32_t (&v)[16], int c0) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) stg[row * 17 + j] = v[j];
+          for (int j = 0; j < 16; ++j) stg[row * 17 + j] = __uint_as_float(v[j]);
           named_bar_sync(1, 128);
           if constexpr (DIRECT) {
             // column = token: pair j of the tile takes its token's column
@@ -370,6 +386,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
           }
           named_bar_sync(1, 128);
+        };
+        uint32_t va[16], vb[16];
+        tmem_ld16_issue(ta, va);
+        tmem_ld_wait();
+        tmem_ld_tie(va);
+        for (int c0 = 0; c0 < ncols; c0 += 32) {
+          if (c0 + 16 < ncols) tmem_ld16_issue(ta + c0 + 16, vb);
+          block(va, c0);
+          tmem_ld_wait();
+          tmem_ld_tie(vb);
+          if (c0 + 16 < ncols) {
+            if (c0 + 32 < ncols) tmem_ld16_issue(ta + c0 + 32, va);
+            block(vb, c0 + 16);
+            tmem_ld_wait();
+            tmem_ld_tie(va);
+          }
         }
       }
       tc_fence_before();
@@ -579,17 +611,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         break;
       }
       tc_fence_after();
+      // Two 16-column register blocks in turn: the next block's TMEM load is in
+      // flight while the current one is stored.
       for (int mt = 0; mt < nv; ++mt) {
         const int h = (tl.m * MT + mt) * 128 + row;
-        for (int c0 = 0; c0 < tl.n; c0 += 16) {
-          float v[16];
-          tmem_ld16(tbase + (static_cast<uint32_t>(32 * q) << 16) +
-                        static_cast<uint32_t>((acc * MT + mt) * N + c0), v);
+        const uint32_t ta = tbase + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>((acc * MT + mt) * N);
+        uint32_t va[16], vb[16];
+        tmem_ld16_issue(ta, va);
+        tmem_ld_wait();
+        tmem_ld_tie(va);
+        for (int c0 = 0; c0 < tl.n; c0 += 32) {
+          if (c0 + 16 < tl.n) tmem_ld16_issue(ta + c0 + 16, vb);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int col = c0 + j;
-            if (col < tl.n) y[static_cast<size_t>(s_pair[col]) * H + h] = s_wt[col] * v[j];
-          }
+          for (int j = 0; j < 16; ++j)
+            if (c0 + j < tl.n) y[static_cast<size_t>(s_pair[c0 + j]) * H + h] = s_wt[c0 + j] * __uint_as_float(va[j]);
+          tmem_ld_wait();
+          tmem_ld_tie(vb);
+          if (c0 + 32 < tl.n) tmem_ld16_issue(ta + c0 + 32, va);
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (c0 + 16 + j < tl.n)
+              y[static_cast<size_t>(s_pair[c0 + 16 + j]) * H + h] = s_wt[c0 + 16 + j] * __uint_as_float(vb[j]);
+          tmem_ld_wait();
+          tmem_ld_tie(va);
         }
       }
       tc_fence_before();
