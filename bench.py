@@ -273,10 +273,11 @@ def run_reference(args, wl, ws_, rank):
     print(json.dumps(line), flush=True)
 
 
-def config_of(wl):
+def config_of(wl, T=None):
     return {"workload": f"{wl.name}: H={wl.hidden} E={wl.n_experts} top-{wl.top_k} I={wl.inter} "
                         f"shared I={wl.shared_inter}{' +sigmoid gate' if wl.has_shared_gate else ''} "
-                        f"{'fp16' if wl.dtype == 1 else 'bf16'} T={wl.T}, {wl.layers} layers rotated",
+                        f"{'fp16' if wl.dtype == 1 else 'bf16'} T={wl.T if T is None else T}, "
+                        f"{wl.layers} layers rotated",
             "T": 1, "layers": wl.layers, "global_batch": 1, "seq_len": 1,
             "parallelism": "replicas",
             "l2": f"inputs larger than L2: {wl.layers} layers x {wl.layer_bytes() / 1e6:.0f} MB of weights, "
@@ -651,7 +652,7 @@ def run_grouped(args, wl, ws_n, rank, local):
         "metric": f"MoE grouped layer µs & achieved HBM GB/s at T={T}; tokens/s", "value": T * K * ws_n / (ms_max / 1e3),
         "unit": "tokens/s", "n_gpus": ws_n, "steps": K, "warmup": W, "ms_per_step": ms_max / K,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded)", "config": {**config_of(wl), "T": T, "path": path,
+        "data": "synthetic (seeded)", "config": {**config_of(wl, T), "T": T, "path": path,
                                                  "mean_distinct_experts": sum(distinct) / L},
         "us_per_layer": us_layer, "hbm_gbs": achieved, "hbm_frac_of_peak": achieved / peak,
         "kernels_per_layer": kpl,
