@@ -109,6 +109,10 @@ WsLayout ws_layout(const moe_cfg_t& c, int32_t T) {
       off = align_up(off + static_cast<size_t>(L.tc_max2) * 16, kWsAlign);
       L.tc_xs = off;
       off = align_up(off + static_cast<size_t>(P) * H * 2, kWsAlign);
+      L.tc_cnt = off;
+      off = align_up(off + static_cast<size_t>(E) * 4, kWsAlign);
+      L.tc_rank = off;
+      off = align_up(off + static_cast<size_t>(T) * k * 4, kWsAlign);
       const int64_t Imax = I > Is ? I : Is;
       L.tc_act_hi = off;
       off = align_up(off + static_cast<size_t>(P) * Imax * 2, kWsAlign);

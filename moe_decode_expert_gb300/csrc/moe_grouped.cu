@@ -230,9 +230,14 @@ moe_status_t launch_grouped(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws,
   // small batches on the tensor-core path: ranking, grouping and tile lists in
   // one single-CTA launch, a warp per token
   const bool fused = use_tc && T <= kRouteGroupMaxT && E <= 256;
+  // larger batches on the tensor-core path: the top-k kernel ranks each pair
+  // within its expert, and the pass launcher files them (no counting sort)
+  const bool ranked = use_tc && !fused;
   int nsplit = -1;
   if (moe_status_t s = launch_router(c, p.x, p.router_w, p.shared_gate_w, T, p.topk_ids, p.topk_w,
-                                     nullptr, ws, L, st, fused ? &nsplit : nullptr))
+                                     nullptr, ws, L, st, fused ? &nsplit : nullptr,
+                                     ranked ? reinterpret_cast<int32_t*>(ws + L.tc_cnt) : nullptr,
+                                     ranked ? reinterpret_cast<int32_t*>(ws + L.tc_rank) : nullptr))
     return s;
   int32_t* counts = reinterpret_cast<int32_t*>(ws + L.g_counts);
   int32_t* offsets = reinterpret_cast<int32_t*>(ws + L.g_offsets);
@@ -244,7 +249,7 @@ moe_status_t launch_grouped(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws,
   const int gate_stride = c.has_shared_gate ? E + 1 : E;
   const int Imax = I > Is ? I : Is;
 
-  if (!fused) {
+  if (!fused && !ranked) {
     launch_pdl(group_kernel, dim3(1), dim3(1024), 0, st, p.topk_ids, T, k, E, Is > 0, counts, offsets, perm, tiles,
                use_tc ? 0 : 1, ctrl);
     if (moe_status_t s = check_launch("group_kernel")) return s;

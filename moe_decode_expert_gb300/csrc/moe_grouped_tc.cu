@@ -801,16 +801,57 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
-// ===================================================== schedule + gather
-// Tile lists of both passes from the per-expert counts/offsets (one CTA).
-// Layout of `sched`: [0] n13, [1] n2, then TcTile arrays at the offsets given.
-__global__ void __launch_bounds__(1024) tc_schedule_kernel(const int32_t* counts,
-                                                           const int32_t* offsets, int E, int I,
-                                                           int Is, int H, int N, int mt13, int mt2, int32_t* n13,
-                                                           int32_t* n2, TcTile* t13, TcTile* t2) {
+// ================================================ grouping, schedule + gather
+// Layout of `sched`: [0] n13, [1] n2 (tile counts of the two passes), [2] / [3]
+// their dynamic tile counters; the TcTile lists sit at their own offsets.
+
+// Grouping from ranks (T > kRouteGroupMaxT): the top-k kernel gave every
+// routed pair its rank within its expert and left the totals in cnt.  Every
+// CTA scans the totals itself and files its share of the pairs (pair p of
+// expert e at offsets[e] + rank[p]; the shared expert's pair of token t at
+// offsets[E] + t); CTA 0 also writes both tile lists.  One launch over many
+// SMs instead of a single-CTA counting sort and a schedule launch.
+__global__ void __launch_bounds__(1024) tc_fill_kernel(const int32_t* ids, const int32_t* rank, const int32_t* cnt,
+                                                       int T, int k, int E, int has_shared, int32_t* perm, int I,
+                                                       int Is, int H, int N, int mt13, int mt2, int32_t* n13,
+                                                       int32_t* n2, TcTile* t13, TcTile* t2) {
   pdl_launch_dependents();  // let the next kernel on the stream launch early
   pdl_wait();               // inputs written by the previous kernel are visible
-  schedule_stage(counts, offsets, E, I, Is, H, N, mt13, mt2, n13, n2, t13, t2);
+  __shared__ int32_t s_cnt[1026], s_off[1026];
+  __shared__ int32_t wsum[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n = E + 1;  // experts + the shared expert (n <= 1025: two per thread)
+  const int e0 = 2 * tid, e1 = 2 * tid + 1;
+  const int c0 = e0 < n ? (e0 < E ? cnt[e0] : (has_shared ? T : 0)) : 0;
+  const int c1 = e1 < n ? (e1 < E ? cnt[e1] : (has_shared ? T : 0)) : 0;
+  int incl = c0 + c1;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int v = wsum[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += y;
+    }
+    wsum[lane] = v;
+  }
+  __syncthreads();
+  const int before = incl - (c0 + c1) + (warp ? wsum[warp - 1] : 0);
+  if (e0 < n) { s_cnt[e0] = c0; s_off[e0] = before; }
+  if (e1 < n) { s_cnt[e1] = c1; s_off[e1] = before + c0; }
+  __syncthreads();
+  if (blockIdx.x == 0) schedule_stage(s_cnt, s_off, E, I, Is, H, N, mt13, mt2, n13, n2, t13, t2);
+  const int np = T * k, P = np + (has_shared ? T : 0);
+  for (int p = blockIdx.x * 1024 + tid; p < P; p += gridDim.x * 1024) {
+    if (p < np) perm[s_off[ids[p]] + rank[p]] = p;
+    else perm[s_off[E] + (p - np)] = p;
+  }
 }
 
 // Small batches (T <= 32, E <= 256): the ranking of every token, the counting
@@ -881,11 +922,15 @@ __global__ void __launch_bounds__(1024) route_group_kernel(float* logits, const 
 }
 
 // Xs[pos, :] = x[token of perm[pos], :]: one warp per row, 16-byte chunks,
-// up to 8 chunks per lane in flight.
+// up to 8 chunks per lane in flight.  CTA 0 also zeroes the E pair counters
+// of the ranked grouping (read by the launch before this one) for the next call.
 __global__ void __launch_bounds__(256) tc_gather_kernel(const uint8_t* x, const int32_t* perm,
-                                                        int P, int T, int k, int H, uint8_t* __restrict__ xs) {
+                                                        int P, int T, int k, int H, uint8_t* __restrict__ xs,
+                                                        int32_t* zero_cnt, int E) {
   pdl_launch_dependents();  // let the next kernel on the stream launch early
   pdl_wait();               // inputs written by the previous kernel are visible
+  if (zero_cnt && blockIdx.x == 0)
+    for (int e = threadIdx.x; e < E; e += 256) zero_cnt[e] = 0;
   const int lane = threadIdx.x & 31;
   const int warps = gridDim.x * 8;
   const int nch = H >> 3;
@@ -1013,10 +1058,14 @@ static moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uin
                fused_nsplit, T, E, E1, k, c.norm_topk, p.topk_ids, p.topk_w, Is > 0 ? 1 : 0, counts, offsets, perm,
                ctrl, I, Is, H, N, mt13, mt2, sched, sched + 1, t13, t2);
     if (moe_status_t s = check_launch("route_group_kernel")) return s;
-  } else {
-    launch_pdl(tc_schedule_kernel, dim3(1), dim3(1024), 0, st, counts, offsets, E, I, Is, H, N, mt13, mt2, sched,
-               sched + 1, t13, t2);
-    if (moe_status_t s = check_launch("tc_schedule_kernel")) return s;
+  } else {  // pairs ranked by the top-k kernel
+    int32_t* cnt = reinterpret_cast<int32_t*>(ws + L.tc_cnt);
+    const int32_t* rank = reinterpret_cast<const int32_t*>(ws + L.tc_rank);
+    const int P1024 = (P + 1023) / 1024;
+    const int gf = P1024 < sm_count() ? P1024 : sm_count();
+    launch_pdl(tc_fill_kernel, dim3(gf > 0 ? gf : 1), dim3(1024), 0, st, p.topk_ids, rank, cnt, T, k, E,
+               Is > 0 ? 1 : 0, perm, I, Is, H, N, mt13, mt2, sched, sched + 1, t13, t2);
+    if (moe_status_t s = check_launch("tc_fill_kernel")) return s;
   }
   const int sms = sm_count();
   // Up to 16 tokens the W13 pass reads x itself (B = all T tokens, each pair
@@ -1027,7 +1076,8 @@ static moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uin
   const bool direct = T <= 16 && T <= N;
   if (!direct) {
     const int gg = (P + 7) / 8 < sms * 8 ? (P + 7) / 8 : sms * 8;
-    launch_pdl(tc_gather_kernel, dim3(gg), dim3(256), 0, st, static_cast<const uint8_t*>(p.x), perm, P, T, k, H, xs);
+    launch_pdl(tc_gather_kernel, dim3(gg), dim3(256), 0, st, static_cast<const uint8_t*>(p.x), perm, P, T, k, H, xs,
+               fused_nsplit >= 0 ? nullptr : reinterpret_cast<int32_t*>(ws + L.tc_cnt), E);
     if (moe_status_t s = check_launch("tc_gather_kernel")) return s;
   }
 

@@ -44,6 +44,8 @@ struct WsLayout {
   size_t tc_tiles13 = 0;  // [tc_max13] tiles of the W13 pass
   size_t tc_tiles2 = 0;   // [tc_max2] tiles of the W2 pass
   size_t tc_xs = 0;       // [P, H] x rows gathered in expert order
+  size_t tc_cnt = 0;      // [E] int32 pair counters (zero between calls) of the ranked grouping
+  size_t tc_rank = 0;     // [T * k] int32: each pair's rank within its expert
   size_t tc_act_hi = 0;   // [P, max(I, Is)] activation, leading term
   size_t tc_act_lo = 0;   // [P, max(I, Is)] activation, remainder term
   // single-launch batch kernel (2 <= T <= kBatchMaxT): exchange words
@@ -106,10 +108,12 @@ moe_status_t launch_decode_fused(const moe_cfg_t& c, const BlockPtrs& p, uint8_t
                                  const WsLayout& L, cudaStream_t st);
 // With nsplit_out != NULL the top-k launch is skipped and *nsplit_out tells
 // how the logits were left (split partial sums, or 0: plain [T, E1] rows).
+// With cnt != NULL the top-k kernel also ranks every pair within its expert:
+// rank[t * k + j] = atomicAdd(&cnt[ids[t * k + j]], 1) (cnt zero beforehand).
 moe_status_t launch_router(const moe_cfg_t& c, const void* x, const void* router_w,
                            const void* shared_gate_w, int32_t T, int32_t* ids, float* w,
                            float* logits_out, uint8_t* ws, const WsLayout& L, cudaStream_t st,
-                           int* nsplit_out = nullptr);
+                           int* nsplit_out = nullptr, int32_t* cnt = nullptr, int32_t* rank = nullptr);
 moe_status_t launch_grouped(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws, const WsLayout& L,
                             int32_t T, cudaStream_t st);
 moe_status_t launch_wait_test(uint8_t* ws, cudaStream_t st);

@@ -243,10 +243,13 @@ __global__ void __launch_bounds__(256) router_mma_kernel(const uint8_t* x,
 // (router_mma_kernel): they are added in split order, stored into `logits`
 // (the [T, E1] buffer later kernels read) and ranked from shared memory.
 // One warp per token: rank, weights, outputs.
+// With cnt != NULL each pair also takes its rank within its expert from a
+// global counter per expert (the order within an expert is arbitrary).
 template <int MAXM>
 __global__ void __launch_bounds__(256) router_topk_kernel(float* logits, const float* part,
                                                           int nsplit, int T, int E, int E1, int k, int norm_topk,
-                                                          int32_t* ids, float* w, float* logits_out) {
+                                                          int32_t* ids, float* w, float* logits_out, int32_t* cnt,
+                                                          int32_t* rank) {
   pdl_launch_dependents();  // let the next kernel on the stream launch early
   pdl_wait();               // inputs written by the previous kernel are visible
   __shared__ int s_ids[8][32];
@@ -258,12 +261,14 @@ __global__ void __launch_bounds__(256) router_topk_kernel(float* logits, const f
   if (t >= T) return;
   topk_token_stage<MAXM>(logits, part, nsplit, t, T, E, E1, k, norm_topk, ids, w, logits_out, s_ids[warp],
                          s_sel[warp], s_w[warp], s_row[warp]);
+  if (cnt && (threadIdx.x & 31) < k)
+    rank[static_cast<size_t>(t) * k + (threadIdx.x & 31)] = atomicAdd(&cnt[s_ids[warp][threadIdx.x & 31]], 1);
 }
 
 moe_status_t launch_router(const moe_cfg_t& c, const void* x, const void* router_w,
                            const void* shared_gate_w, int32_t T, int32_t* ids, float* w,
                            float* logits_out, uint8_t* ws, const WsLayout& L, cudaStream_t st,
-                           int* nsplit_out) {
+                           int* nsplit_out, int32_t* cnt, int32_t* rank) {
   const int E = c.n_experts;
   const int E1 = E + 1;
   float* lg = reinterpret_cast<float*>(ws + L.r_logits);
@@ -317,9 +322,11 @@ moe_status_t launch_router(const moe_cfg_t& c, const void* x, const void* router
   // The logits rows are laid out with stride E1 only when the gate column exists.
   dim3 g2((T + 7) / 8);
   if (E <= 256)
-    launch_pdl(router_topk_kernel<8>, dim3(g2), dim3(256), 0, st, lg, reinterpret_cast<const float*>(ws + L.r_part), nsplit, T, E, stride, c.top_k, c.norm_topk, ids, w, logits_out);
+    launch_pdl(router_topk_kernel<8>, dim3(g2), dim3(256), 0, st, lg, reinterpret_cast<const float*>(ws + L.r_part),
+               nsplit, T, E, stride, c.top_k, c.norm_topk, ids, w, logits_out, cnt, rank);
   else
-    launch_pdl(router_topk_kernel<32>, dim3(g2), dim3(256), 0, st, lg, static_cast<const float*>(nullptr), 0, T, E, stride, c.top_k, c.norm_topk, ids, w, logits_out);
+    launch_pdl(router_topk_kernel<32>, dim3(g2), dim3(256), 0, st, lg, static_cast<const float*>(nullptr), 0, T, E,
+               stride, c.top_k, c.norm_topk, ids, w, logits_out, cnt, rank);
   if (moe_status_t s = check_launch("router_topk_kernel")) return s;
   stat_kernels(2);
   return MOE_OK;

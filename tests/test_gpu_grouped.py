@@ -77,8 +77,8 @@ def test_small_batch_zipf(m, T, flags):
 @pytest.mark.parametrize("T", [9, 16, 17, 31, 32, 33])
 def test_small_batch_fused_ranking_boundary(m, T):
     """Up to 32 tokens one single-CTA launch ranks (a warp per token), groups
-    and lists the tiles; from 33 on the ranking, grouping and tile lists are
-    three launches.  Up to 16 tokens the W13 pass reads x itself (no gather
+    and lists the tiles; from 33 on the top-k launch also ranks each pair
+    within its expert and one launch files the pairs and lists the tiles.  Up to 16 tokens the W13 pass reads x itself (no gather
     launch).  Both sides of the boundaries, and ragged counts, match the
     oracle."""
     wl = moe_synth.workload("small_batch")
@@ -87,9 +87,9 @@ def test_small_batch_fused_ranking_boundary(m, T):
     ids, w, out = _grouped(m, wl, g, T, flags=TC)
     st = m.moe_get_stats()
     assert st["grouped_tc_calls"] == 1
-    # router (+ top-k), ranking/grouping/tile lists (1 or 3), gather (0 or 1),
-    # W13, W2, combine
-    expect = (1 + 1 if T <= 32 else 2 + 2) + (0 if T <= 16 else 1) + 3
+    # router (+ top-k), ranking/grouping/tile lists (1) or filing/tile lists
+    # (1), gather (0 or 1), W13, W2, combine
+    expect = (1 + 1 if T <= 32 else 2 + 1) + (0 if T <= 16 else 1) + 3
     assert st["kernels_launched"] == expect
     tokens = list(range(T))  # every token
     check_tokens(ids, w, out, _ref_tokens(wl, 2, T, g, tokens), tokens, wl.top_k)
@@ -120,6 +120,26 @@ def test_token_permutation_permutes_output(m, flags):
     g2["x"] = g["x"][perm].contiguous()
     _, _, out2 = _grouped(m, wl, g2, T, flags=flags)
     assert torch.equal(out2, out[perm])
+
+
+def test_ranked_grouping_repeats_on_one_workspace(m):
+    """From 33 tokens the top-k launch ranks pairs with per-expert counters
+    that a later launch of the same call zeroes again: calls repeated on one
+    workspace, with a small batch in between, give the same bits."""
+    wl = moe_synth.workload("small_batch")
+    T = 100
+    g = moe_synth.make_layer(wl, 8, T, device=DEV)
+    g8 = moe_synth.make_layer(wl, 9, 8, device=DEV)
+    cfg = m.cfg_from_workload(wl, None, TC)
+    ws = m.alloc_workspace(cfg, T, DEV)
+    first = _grouped(m, wl, g, T, flags=TC, ws=ws)
+    tokens = list(range(0, T, 7))
+    check_tokens(*first, _ref_tokens(wl, 8, T, g, tokens), tokens, wl.top_k)
+    for _ in range(2):
+        _grouped(m, wl, g8, 8, flags=TC, ws=ws)
+        again = _grouped(m, wl, g, T, flags=TC, ws=ws)
+        for a, b in zip(first, again):
+            assert torch.equal(a, b)
 
 
 def test_tcgen05_path_rejects_fp16(m):

@@ -36,7 +36,7 @@ def _kernel_signatures(text):
 def test_kernels_found():
     names = {n for src in _sources().values() for n, _ in _kernel_signatures(src)}
     for k in ("decode_fused_kernel", "route_group_kernel", "tc_w13_kernel", "tc_w2_kernel", "combine_kernel",
-              "router_mma_kernel", "router_topk_kernel", "group_kernel"):
+              "router_mma_kernel", "router_topk_kernel", "group_kernel", "tc_fill_kernel"):
         assert k in names, k
 
 
