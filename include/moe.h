@@ -26,7 +26,8 @@
  * --------------------------------
  *  * All tensor pointers are DEVICE pointers owned by the caller, row-major and
  *    contiguous, 16-byte aligned.  The library keeps no pointer after a call
- *    returns and allocates no device memory.
+ *    returns and allocates no device memory at run time (the allocation-free
+ *    entry's scratch array below is a fixed module symbol).
  *  * Shapes: x [T, H]; router_w [E, H]; w13 [E, 2I, H] (gate rows then up
  *    rows); w2 [E, H, I]; shared_w13 [2Is, H]; shared_w2 [H, Is];
  *    shared_gate_w [H]; out [T, H] in cfg->out_dtype; topk.ids [T, k] int32;
