@@ -76,7 +76,12 @@ WsLayout ws_layout(const moe_cfg_t& c, int32_t T) {
   L.r_logits = off;
   off = align_up(off + static_cast<size_t>(T) * (E + 1) * 4, kWsAlign);
   L.r_part = off;
-  if (T <= 64) off = align_up(off + static_cast<size_t>(H / 256 + 1) * T * (E + 1) * 4, kWsAlign);
+  if (T <= 64) {
+    off = align_up(off + static_cast<size_t>(H / 256 + 1) * T * (E + 1) * 4, kWsAlign);
+  } else if (T >= kRouterTcMinT && E <= 256) {  // the tensor-core router's K-split partial sums
+    L.r_part_splits = kRouterMaxSplits;
+    off = align_up(off + static_cast<size_t>(kRouterMaxSplits) * T * (E + 1) * 4, kWsAlign);
+  }
   if (T > 1) {
     const int64_t P = T * k + (Is > 0 ? T : 0);
     const int64_t tn = 8;  // pairs per tile of the grouped kernels

@@ -39,6 +39,10 @@ constexpr int kTcThreads = 192;
 constexpr int kBK = 64;                 // K elements per stage: one 128-byte swizzle row
 constexpr uint32_t kTileA = 128 * 128;  // 128 rows x 128 bytes
 constexpr int kSmemBudget = 220 * 1024;
+// Ranked grouping: up to this many pairs the filing launch also copies the x
+// rows (T = 64 / 512: 1.0 / 2.6 us less per layer); beyond, a gather launch
+// with twice the warps per SM copies them faster (T = 4096: 2.7 us).
+constexpr int kFoldGatherMaxPairs = 16384;
 
 
 // ----------------------------------------------------------------- PTX
@@ -181,7 +185,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                   const __grid_constant__ CUtensorMap mapB, const TcTile* tiles,
                   const int32_t* n_tiles_p, int H, int I, int Is, int E, int act_stride,
                   uint16_t* __restrict__ act_hi, uint16_t* __restrict__ act_lo, Control* ctrl, uint64_t timeout,
-                  const int32_t* perm, int direct_T, int k, int32_t* tile_ctr) {
+                  const int32_t* perm, int direct_T, int k, int32_t* tile_ctr, int32_t* zero_cnt, int zero_n) {
   pdl_launch_dependents();  // let the next kernel on the stream launch early
   constexpr uint32_t kStage = MT * kTileA + N * 128;
   constexpr int kStg = 128 * 17 * 4;
@@ -221,6 +225,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t tbase = tmem_base_s;
   const int ntiles = *n_tiles_p;
   const int KB = H / kBK;
+  // the ranked grouping's per-expert counters, read by the filing launch before
+  // this one, start the next call at zero
+  if (zero_cnt && blockIdx.x == 0)
+    for (int e = threadIdx.x; e < zero_n; e += kTcThreads) zero_cnt[e] = 0;
 
   if (warp == 0) {
     if (lane == 0) {  // ---------------------------------------------- TMA producer
@@ -653,12 +661,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // logits[t, e] = x[t] . Wr[e] for T tokens on tcgen05: router rows are M (128
 // per tile), tokens N (128), K = H.  M-tiles [0, mE) cover the E router rows;
 // with a shared gate one more M-tile reads the gate vector as a one-row tensor
-// (TMA fills the other 127 rows with zeros).  Tile t: m = t % nm, n = t / nm.
+// (TMA fills the other 127 rows with zeros).  K is split S ways when the
+// tiles would leave SMs idle: split s adds K blocks [s KB/S, (s+1) KB/S) and,
+// with S > 1, writes its partial sums to part + s T E1 (the top-k kernel adds
+// the S partials in split order).  Tile t: m = t % nm, then s, then n.
 template <int DT, int N>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_router_kernel(const __grid_constant__ CUtensorMap mapWr, const __grid_constant__ CUtensorMap mapG,
                      const __grid_constant__ CUtensorMap mapX, int T, int H, int E, int E1, int mE, int nm,
-                     float* __restrict__ logits, Control* ctrl, uint64_t timeout) {
+                     int S, float* __restrict__ logits, Control* ctrl, uint64_t timeout) {
   pdl_launch_dependents();  // let the next kernel on the stream launch early
   constexpr uint32_t kStage = kTileA + N * 128;
   constexpr int kStages = kSmemBudget / kStage > 8 ? 8 : kSmemBudget / kStage;
@@ -690,8 +701,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // tile list and the operands it wrote are read.
   pdl_wait();
   const uint32_t tbase = tmem_base_s;
-  const int ntiles = nm * ((T + N - 1) / N);
-  const int KB = H / kBK;
+  const int ntiles = nm * S * ((T + N - 1) / N);
+  const int KB = H / kBK / S;  // K blocks per split
 
   if (warp == 0) {
     if (lane == 0) {
@@ -699,9 +710,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       uint32_t phase = 0;
       uint32_t issued_mask = 0, issued_phase = 0;
       for (int t = blockIdx.x; t < ntiles && !s_abort; t += gridDim.x) {
-        const int m = t % nm, n = t / nm;
+        const int m = t % nm, sp = (t / nm) % S, n = t / (nm * S);
         const bool gate = m >= mE;
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int kb = sp * KB; kb < (sp + 1) * KB; ++kb) {
           if (!tc_wait(&empty[stage], phase ^ 1u, timeout, &s_abort)) {
             s_abort = 1;
             report_error(ctrl, kDevTimeoutCopy, blockIdx.x);
@@ -764,7 +775,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int row = 32 * q + lane;
     int it = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
-      const int m = t % nm, n = t / nm;
+      const int m = t % nm, sp = (t / nm) % S, n = t / (nm * S);
+      float* dst = logits + static_cast<size_t>(sp) * T * E1;
       const int acc = it & 1;
       const bool ok = !s_abort && tc_wait(&tfull[acc], (it >> 1) & 1, timeout, &s_abort);
       if (epi_any(!ok)) {
@@ -784,7 +796,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int tok = n * N + c0 + j;
-            if (tok < T) logits[static_cast<size_t>(tok) * E1 + e] = v[j];
+            if (tok < T) dst[static_cast<size_t>(tok) * E1 + e] = v[j];
           }
         }
       }
@@ -808,13 +820,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // Grouping from ranks (T > kRouteGroupMaxT): the top-k kernel gave every
 // routed pair its rank within its expert and left the totals in cnt.  Every
 // CTA scans the totals itself and files its share of the pairs (pair p of
-// expert e at offsets[e] + rank[p]; the shared expert's pair of token t at
-// offsets[E] + t); CTA 0 also writes both tile lists.  One launch over many
-// SMs instead of a single-CTA counting sort and a schedule launch.
+// expert e at position offsets[e] + rank[p]; the shared expert's pair of token
+// t at offsets[E] + t); CTA 0 also writes both tile lists.  With xs set it
+// files a pair per warp and copies the pair's x row to Xs[pos] on the way (no
+// gather launch), else a pair per thread.  One launch over many SMs instead of
+// a single-CTA counting sort and a schedule launch.
 __global__ void __launch_bounds__(1024) tc_fill_kernel(const int32_t* ids, const int32_t* rank, const int32_t* cnt,
                                                        int T, int k, int E, int has_shared, int32_t* perm, int I,
                                                        int Is, int H, int N, int mt13, int mt2, int32_t* n13,
-                                                       int32_t* n2, TcTile* t13, TcTile* t2) {
+                                                       int32_t* n2, TcTile* t13, TcTile* t2, const uint8_t* x,
+                                                       uint8_t* __restrict__ xs) {
   pdl_launch_dependents();  // let the next kernel on the stream launch early
   pdl_wait();               // inputs written by the previous kernel are visible
   __shared__ int32_t s_cnt[1026], s_off[1026];
@@ -848,9 +863,33 @@ __global__ void __launch_bounds__(1024) tc_fill_kernel(const int32_t* ids, const
   __syncthreads();
   if (blockIdx.x == 0) schedule_stage(s_cnt, s_off, E, I, Is, H, N, mt13, mt2, n13, n2, t13, t2);
   const int np = T * k, P = np + (has_shared ? T : 0);
-  for (int p = blockIdx.x * 1024 + tid; p < P; p += gridDim.x * 1024) {
-    if (p < np) perm[s_off[ids[p]] + rank[p]] = p;
-    else perm[s_off[E] + (p - np)] = p;
+  if (!xs) {
+    for (int p = blockIdx.x * 1024 + tid; p < P; p += gridDim.x * 1024) {
+      if (p < np) perm[s_off[ids[p]] + rank[p]] = p;
+      else perm[s_off[E] + (p - np)] = p;
+    }
+    return;
+  }
+  const int nch = H >> 3;  // 16-byte chunks per x row
+  for (int p = blockIdx.x * 32 + warp; p < P; p += gridDim.x * 32) {
+    int pos = 0;
+    if (lane == 0) {
+      pos = p < np ? s_off[ids[p]] + rank[p] : s_off[E] + (p - np);
+      perm[pos] = p;
+    }
+    pos = __shfl_sync(0xffffffffu, pos, 0);
+    const int t = p < np ? p / k : p - np;
+    const uint8_t* src = x + static_cast<size_t>(t) * H * 2;
+    uint8_t* dst = xs + static_cast<size_t>(pos) * H * 2;
+    for (int c0 = lane; c0 < nch; c0 += 32 * 8) {
+      uint4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (c0 + 32 * u < nch) v[u] = ld_nc16(src + 16 * (c0 + 32 * u));
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (c0 + 32 * u < nch) *reinterpret_cast<uint4*>(dst + 16 * (c0 + 32 * u)) = v[u];
+    }
   }
 }
 
@@ -922,15 +961,12 @@ __global__ void __launch_bounds__(1024) route_group_kernel(float* logits, const 
 }
 
 // Xs[pos, :] = x[token of perm[pos], :]: one warp per row, 16-byte chunks,
-// up to 8 chunks per lane in flight.  CTA 0 also zeroes the E pair counters
-// of the ranked grouping (read by the launch before this one) for the next call.
+// up to 8 chunks per lane in flight (17 to 32 tokens; from 33 the filing
+// launch copies the rows).
 __global__ void __launch_bounds__(256) tc_gather_kernel(const uint8_t* x, const int32_t* perm,
-                                                        int P, int T, int k, int H, uint8_t* __restrict__ xs,
-                                                        int32_t* zero_cnt, int E) {
+                                                        int P, int T, int k, int H, uint8_t* __restrict__ xs) {
   pdl_launch_dependents();  // let the next kernel on the stream launch early
   pdl_wait();               // inputs written by the previous kernel are visible
-  if (zero_cnt && blockIdx.x == 0)
-    for (int e = threadIdx.x; e < E; e += 256) zero_cnt[e] = 0;
   const int lane = threadIdx.x & 31;
   const int warps = gridDim.x * 8;
   const int nch = H >> 3;
@@ -1061,10 +1097,16 @@ static moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uin
   } else {  // pairs ranked by the top-k kernel
     int32_t* cnt = reinterpret_cast<int32_t*>(ws + L.tc_cnt);
     const int32_t* rank = reinterpret_cast<const int32_t*>(ws + L.tc_rank);
-    const int P1024 = (P + 1023) / 1024;
-    const int gf = P1024 < sm_count() ? P1024 : sm_count();
+    // up to kFoldGatherMaxPairs pairs a warp per pair, copying the x rows too
+    // (one 1024-thread CTA per SM); with more, the copy has a launch of its own
+    // with twice the warps per SM
+    const bool fold = P <= kFoldGatherMaxPairs;
+    const int per = fold ? 32 : 1024;
+    const int gq = (P + per - 1) / per;
+    const int gf = gq < sm_count() ? gq : sm_count();
     launch_pdl(tc_fill_kernel, dim3(gf > 0 ? gf : 1), dim3(1024), 0, st, p.topk_ids, rank, cnt, T, k, E,
-               Is > 0 ? 1 : 0, perm, I, Is, H, N, mt13, mt2, sched, sched + 1, t13, t2);
+               Is > 0 ? 1 : 0, perm, I, Is, H, N, mt13, mt2, sched, sched + 1, t13, t2,
+               static_cast<const uint8_t*>(p.x), fold ? xs : nullptr);
     if (moe_status_t s = check_launch("tc_fill_kernel")) return s;
   }
   const int sms = sm_count();
@@ -1074,10 +1116,10 @@ static moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uin
   // more tokens every CTA reads the same x rows at the same time (8 KB per
   // stage at T = 64, +10 us per layer), so the gathered rows are used.
   const bool direct = T <= 16 && T <= N;
-  if (!direct) {
+  const bool gather = !direct && (fused_nsplit >= 0 || P > kFoldGatherMaxPairs);
+  if (gather) {
     const int gg = (P + 7) / 8 < sms * 8 ? (P + 7) / 8 : sms * 8;
-    launch_pdl(tc_gather_kernel, dim3(gg), dim3(256), 0, st, static_cast<const uint8_t*>(p.x), perm, P, T, k, H, xs,
-               fused_nsplit >= 0 ? nullptr : reinterpret_cast<int32_t*>(ws + L.tc_cnt), E);
+    launch_pdl(tc_gather_kernel, dim3(gg), dim3(256), 0, st, static_cast<const uint8_t*>(p.x), perm, P, T, k, H, xs);
     if (moe_status_t s = check_launch("tc_gather_kernel")) return s;
   }
 
@@ -1102,7 +1144,8 @@ static moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uin
   auto launch13 = [&](auto kernel, size_t s13) {
     cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s13));
     launch_pdl(kernel, dim3(g13 > 0 ? g13 : 1), dim3(kTcThreads), s13, st, mA, mAs, mB, t13, sched, H, I, Is, E,
-               Imax, ahi, alo, ctrl, timeout, perm, direct ? T : 0, k, sched + 2);
+               Imax, ahi, alo, ctrl, timeout, perm, direct ? T : 0, k, sched + 2,
+               fused_nsplit >= 0 ? nullptr : reinterpret_cast<int32_t*>(ws + L.tc_cnt), E);
   };
   if (mt13 == 1) {
     if (direct) launch13(tc_w13_kernel<DT, N, 1, true>, tc_smem13<N, 1>());
@@ -1121,7 +1164,7 @@ static moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uin
   if (mt2 == 1) launch2(tc_w2_kernel<DT, N, 1>, tc_smem2<N, 1>());
   else launch2(tc_w2_kernel<DT, N, kMT>, tc_smem2<N, kMT>());
   if (moe_status_t s = check_launch("tc_w2_kernel")) return s;
-  stat_kernels(direct ? 3 : 4);
+  stat_kernels(gather ? 4 : 3);
   return MOE_OK;
 }
 
@@ -1132,7 +1175,8 @@ bool tc_router_supported(const moe_cfg_t& c) {
 
 // logits [T, E1] (E1 = E, or E + 1 with the gate column) on tensor cores.
 moe_status_t launch_tc_router(const moe_cfg_t& c, const void* x, const void* router_w, const void* gate_w,
-                              int32_t T, float* logits, int E1, Control* ctrl, cudaStream_t st) {
+                              int32_t T, float* logits, float* part, int E1, Control* ctrl, cudaStream_t st,
+                              int* nsplit) {
   constexpr int DT = MOE_BF16, N = 128;
   const int H = c.hidden, E = c.n_experts;
   const int mE = (E + 127) / 128;
@@ -1146,11 +1190,24 @@ moe_status_t launch_tc_router(const moe_cfg_t& c, const void* x, const void* rou
   constexpr int ns = kSmemBudget / st_bytes > 8 ? 8 : kSmemBudget / st_bytes;
   const size_t smem = static_cast<size_t>(ns) * st_bytes + 1024;
   cudaFuncSetAttribute(tc_router_kernel<DT, N>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  const int tiles = nm * ((T + N - 1) / N);
+  const int tiles0 = nm * ((T + N - 1) / N);
   const int sms = sm_count();
+  // K splits when the tiles would leave most SMs idle (T = 512: 12 tiles, 5.4
+  // us less per layer; at T = 4096, 96 tiles, four splits cost 4 us in partial
+  // sums): the fewest rounds of (K blocks per split + 2 for the epilogue)
+  int S = 1;
+  if (part && E <= 256 && 2 * tiles0 <= sms) {
+    int best = 1 << 30;
+    for (int sp = 1; sp <= kRouterMaxSplits && (H / kBK) % sp == 0; sp *= 2) {
+      const int cost = ((tiles0 * sp + sms - 1) / sms) * (H / kBK / sp + 2);
+      if (cost < best) { best = cost; S = sp; }
+    }
+  }
+  *nsplit = S > 1 ? S : 0;
+  const int tiles = tiles0 * S;
   const int g = tiles < sms ? tiles : sms;
-  launch_pdl(tc_router_kernel<DT, N>, dim3(g), dim3(kTcThreads), smem, st, mWr, mG, mX, T, H, E, E1, mE, nm, logits, ctrl,
-                                                       wait_timeout_ns());
+  launch_pdl(tc_router_kernel<DT, N>, dim3(g), dim3(kTcThreads), smem, st, mWr, mG, mX, T, H, E, E1, mE, nm, S,
+             S > 1 ? part : logits, ctrl, wait_timeout_ns());
   if (moe_status_t s = check_launch("tc_router_kernel")) return s;
   stat_kernels(1);
   return MOE_OK;

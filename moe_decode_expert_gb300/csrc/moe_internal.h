@@ -31,7 +31,9 @@ struct WsLayout {
   size_t ll_act = 0;      // kActReplicas x (k*I + Is) words, each copy padded to even
   // router for T tokens
   size_t r_logits = 0;    // [T, E + 1] fp32 (column E: shared-gate logit)
-  size_t r_part = 0;      // T <= 64: [H / 256 + 1, T, E + 1] fp32 split partial logits
+  size_t r_part = 0;      // T <= 64: [H / 256 + 1, T, E + 1] fp32 split partial logits;
+                          // T >= kRouterTcMinT: [r_part_splits, T, E + 1] (tensor-core router)
+  int r_part_splits = 0;  // K splits the tensor-core router may use (0: none)
   // grouped path (T > 1)
   size_t g_counts = 0;    // (E + 2) int32: tokens per expert (E = shared)
   size_t g_offsets = 0;   // (E + 2) int32: exclusive prefix of counts
@@ -136,8 +138,13 @@ bool tc_path_supported(const moe_cfg_t& c);  // eligibility and the TMA encoder 
 int tc_tile_n(const moe_cfg_t& c, int32_t T);
 struct Control;
 bool tc_router_supported(const moe_cfg_t& c);
+// part: room for kRouterMaxSplits x [T, E1] fp32 partial sums, or NULL (no
+// K split); *nsplit: the splits left in part (0: the logits are in `logits`).
+constexpr int kRouterMaxSplits = 8;
+constexpr int kRouterTcMinT = 256;  // bf16 and T from this on: tensor-core router
 moe_status_t launch_tc_router(const moe_cfg_t& c, const void* x, const void* router_w, const void* gate_w,
-                              int32_t T, float* logits, int E1, Control* ctrl, cudaStream_t st);
+                              int32_t T, float* logits, float* part, int E1, Control* ctrl, cudaStream_t st,
+                              int* nsplit);
 // fused_nsplit >= 0: the router ran without its top-k (logits as that many
 // split partial sums, 0 = plain); ranking, grouping and the tile lists then run
 // as one launch.  -1: ids and the grouping are already in the workspace.

@@ -20,7 +20,6 @@ constexpr int kRBM = 64;   // router rows (experts) per CTA tile
 constexpr int kRBN = 64;   // tokens per CTA tile
 constexpr int kRBK = 32;   // hidden elements per k-step
 constexpr int kRouterGemvMaxT = 64;  // T up to this uses the row-per-warp kernel
-constexpr int kRouterTcMinT = 256;   // bf16 and T from this on: tensor-core router
 
 template <int DT>
 __global__ void __launch_bounds__(256) router_logits_kernel(const uint8_t* x,
@@ -279,8 +278,9 @@ moe_status_t launch_router(const moe_cfg_t& c, const void* x, const void* router
   const bool tc = T >= kRouterTcMinT && tc_router_supported(c);
   int nsplit = 0;  // > 0: the logits are split partial sums (router_mma_kernel)
   if (tc) {
-    if (moe_status_t s = launch_tc_router(c, x, router_w, swg, T, lg, stride,
-                                          reinterpret_cast<Control*>(ws + L.ctrl), st))
+    float* part = L.r_part_splits ? reinterpret_cast<float*>(ws + L.r_part) : nullptr;
+    if (moe_status_t s = launch_tc_router(c, x, router_w, swg, T, lg, part, stride,
+                                          reinterpret_cast<Control*>(ws + L.ctrl), st, &nsplit))
       return s;
   } else if (T <= kRouterGemvMaxT && E1 <= 257 && c.hidden % 8 == 0) {
     const int nm = (stride + 15) / 16;

@@ -78,7 +78,8 @@ def test_small_batch_zipf(m, T, flags):
 def test_small_batch_fused_ranking_boundary(m, T):
     """Up to 32 tokens one single-CTA launch ranks (a warp per token), groups
     and lists the tiles; from 33 on the top-k launch also ranks each pair
-    within its expert and one launch files the pairs and lists the tiles.  Up to 16 tokens the W13 pass reads x itself (no gather
+    within its expert and one launch files the pairs, copies their x rows and
+    lists the tiles.  Up to 16 tokens the W13 pass reads x itself (no gather
     launch).  Both sides of the boundaries, and ragged counts, match the
     oracle."""
     wl = moe_synth.workload("small_batch")
@@ -87,9 +88,10 @@ def test_small_batch_fused_ranking_boundary(m, T):
     ids, w, out = _grouped(m, wl, g, T, flags=TC)
     st = m.moe_get_stats()
     assert st["grouped_tc_calls"] == 1
-    # router (+ top-k), ranking/grouping/tile lists (1) or filing/tile lists
-    # (1), gather (0 or 1), W13, W2, combine
-    expect = (1 + 1 if T <= 32 else 2 + 1) + (0 if T <= 16 else 1) + 3
+    # router (+ top-k), ranking/grouping/tile lists (1) or filing/x rows/tile
+    # lists (1), gather (1 for 17..32 tokens, and past 16384 pairs), W13, W2,
+    # combine
+    expect = (1 + 1 if T <= 32 else 2 + 1) + (1 if 16 < T <= 32 else 0) + 3
     assert st["kernels_launched"] == expect
     tokens = list(range(T))  # every token
     check_tokens(ids, w, out, _ref_tokens(wl, 2, T, g, tokens), tokens, wl.top_k)
