@@ -786,9 +786,9 @@ __global__ void __launch_bounds__(kBtBlock, 1) decode_batch_kernel(const BatchAr
                           static_cast<uint32_t>(lane & 7) * a.gs2 + ((lane >> 3) & 1) * Iu * 2 + (lane >> 4) * 16;
       const uint32_t bb = terms_a + ls * slot_bytes + static_cast<uint32_t>(g) * a.cs + 4 * t4;
       // B column block nc holds columns 8 nc .. 8 nc + 7 (tokens 4 nc .. 4 nc + 3)
-      float acc[NBC][2][4] = {};
+      float acc[NBC][4][4] = {};
       // NK 16-column steps at a time: every operand load issued before the
-      // tensor-core steps, two accumulator chains (static indices: a runtime
+      // tensor-core steps, four accumulator chains (static indices: a runtime
       // index would put the accumulators in local memory)
       auto ksteps = [&](auto nk_c, int ks) {
         constexpr int NK = decltype(nk_c)::value;
@@ -809,7 +809,7 @@ __global__ void __launch_bounds__(kBtBlock, 1) decode_batch_kernel(const BatchAr
 #pragma unroll
           for (int nc = 0; nc < NBC; ++nc)
             if (8 * nc < 2 * T)
-              mma16816<DT>(acc[nc][i & 1], av[i][0], av[i][1], av[i][2], av[i][3], xv[i][nc][0], xv[i][nc][1]);
+              mma16816<DT>(acc[nc][i & 3], av[i][0], av[i][1], av[i][2], av[i][3], xv[i][nc][0], xv[i][nc][1]);
       };
       const int nks = Iu >> 4;
       int ks = 0;
@@ -819,12 +819,12 @@ __global__ void __launch_bounds__(kBtBlock, 1) decode_batch_kernel(const BatchAr
       if (us == 0) MOE_STAMP(19);  // warp 0's first unit computed
       // lane (g, t4): tile rows g, g + 8 (unit rows 2g, 2g + 1) of tokens
       // 4 nc + t4 (columns hi, lo of block nc)
-      auto publish = [&](int tk, const float(&ac)[2][4]) {
+      auto publish = [&](int tk, const float(&ac)[4][4]) {
         if (tk < T && (sh || ((s_utok[s] >> tk) & 1u))) {
           float unsc = 1.0f;
           if constexpr (DT == MOE_F16) unsc = s_unsc[ls][tk];
-          const float y0 = ((ac[0][0] + ac[1][0]) + (ac[0][1] + ac[1][1])) * unsc;
-          const float y1 = ((ac[0][2] + ac[1][2]) + (ac[0][3] + ac[1][3])) * unsc;
+          const float y0 = (((ac[0][0] + ac[1][0]) + (ac[2][0] + ac[3][0])) + ((ac[0][1] + ac[1][1]) + (ac[2][1] + ac[3][1]))) * unsc;
+          const float y1 = (((ac[0][2] + ac[1][2]) + (ac[2][2] + ac[3][2])) + ((ac[0][3] + ac[1][3]) + (ac[2][3] + ac[3][3]))) * unsc;
           uint64_t* pr = a.ll_part + static_cast<size_t>((sh ? SH : s) * T + tk) * H + hb * 16;
           ll_store(pr + 2 * g, y0, epoch);
           ll_store(pr + 2 * g + 1, y1, epoch);
