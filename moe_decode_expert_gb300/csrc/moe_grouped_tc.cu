@@ -961,8 +961,8 @@ __global__ void __launch_bounds__(1024) route_group_kernel(float* logits, const 
 }
 
 // Xs[pos, :] = x[token of perm[pos], :]: one warp per row, 16-byte chunks,
-// up to 8 chunks per lane in flight (17 to 32 tokens; from 33 the filing
-// launch copies the rows).
+// up to 8 chunks per lane in flight.  Used for 17 to 32 tokens and past
+// kFoldGatherMaxPairs pairs; in between the filing launch copies the rows.
 __global__ void __launch_bounds__(256) tc_gather_kernel(const uint8_t* x, const int32_t* perm,
                                                         int P, int T, int k, int H, uint8_t* __restrict__ xs) {
   pdl_launch_dependents();  // let the next kernel on the stream launch early
