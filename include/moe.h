@@ -103,10 +103,10 @@ typedef struct moe_cfg {
 /* cfg->flags bits selecting the T > 1 path (at most one of SIMT, TC and
  * SINGLE).  With none of them the library picks: the single-launch kernel
  * when the shape allows it (E <= 256, top_k <= 8, H a multiple of 256 up to
- * 2048, I and Is multiples of 16) for 2 <= T <= 8, and for T <= 16 when the
- * tcgen05 kernels are not available; else the tcgen05 kernels when the shape
- * allows (bf16, H % 128 == 0, I and Is multiples of 64); else the CUDA-core
- * kernels. */
+ * 2048, I and Is multiples of 16) for 2 <= T <= 8 (T <= 3 when I < 256), and
+ * for T <= 16 when the tcgen05 kernels are not available; else the tcgen05
+ * kernels when the shape allows (H % 128 == 0, I and Is multiples of 64);
+ * else the CUDA-core kernels. */
 #define MOE_FLAG_GROUPED_SIMT 1  /* T > 1 on the CUDA-core grouped kernels      */
 #define MOE_FLAG_GROUPED_TC 2    /* T > 1 on the tcgen05 grouped kernels;
                                     MOE_ERR_UNSUPPORTED if the shape does not allow it */

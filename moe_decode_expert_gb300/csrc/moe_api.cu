@@ -306,11 +306,15 @@ moe_status_t moe_grouped_forward(const moe_cfg_t* cfg, const void* x, const void
   if (static_cast<int64_t>(T) * cfg->top_k > (1 << 30))
     return set_error(MOE_ERR_UNSUPPORTED, "T * top_k too large");
   // 2 <= T <= 16: the single-launch kernel when asked for, or by default when
-  // the shape allows it and no other T > 1 path was asked for: up to 8 tokens,
-  // and up to 16 where the tensor-core passes are not available (measured:
-  // from 9 tokens the tensor-core passes are faster, the CUDA-core ones slower)
+  // the shape allows it and no other T > 1 path was asked for: up to 8 tokens
+  // (3 when I < 256: its W2 units of 16 short rows are copy-issue-bound there),
+  // and up to 16 where the tensor-core passes are not available.  Measured:
+  // I = 512, from 9 tokens the tensor-core passes are faster; I = 128 (fp16),
+  // T = 2 / 4 / 8: 22.1 / 32.8 / 52.2 us against 28.4 / 31.6 / 40.2 there.
   const bool other = cfg->flags & (MOE_FLAG_GROUPED_SIMT | MOE_FLAG_GROUPED_TC);
-  const bool single_default = !other && batch_shape_ok(*cfg, T) && (T <= 8 || !tc_path_supported(*cfg));
+  const int single_max = cfg->inter >= 256 ? 8 : 3;
+  const bool single_default =
+      !other && batch_shape_ok(*cfg, T) && (T <= single_max || !tc_path_supported(*cfg));
   if ((cfg->flags & MOE_FLAG_GROUPED_SINGLE) || single_default) {
     if (moe_status_t s = launch_decode_batch(*cfg, p, static_cast<uint8_t*>(ws), L, T, st)) return s;
     stat_grouped();

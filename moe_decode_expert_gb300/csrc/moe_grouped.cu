@@ -258,7 +258,7 @@ moe_status_t launch_grouped(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws,
 
   const int sms = sm_count();
   if ((c.flags & MOE_FLAG_GROUPED_TC) && !use_tc)
-    return set_error(MOE_ERR_UNSUPPORTED, "grouped: the tensor-core path needs bf16, H %% 128 == 0, "
+    return set_error(MOE_ERR_UNSUPPORTED, "grouped: the tensor-core path needs H %% 128 == 0, "
                                           "I and Is multiples of 64 and the TMA encoder");
   if (use_tc) {
     if (moe_status_t s = launch_tc_passes(c, p, ws, L, T, fused ? nsplit : -1, st)) return s;

@@ -1019,7 +1019,8 @@ static bool make_map(CUtensorMap* m, int dtype, const void* base, uint64_t inner
 }
 
 bool tc_shape_ok(const moe_cfg_t& c) {
-  return c.dtype == MOE_BF16 && c.hidden % 128 == 0 && c.inter % 64 == 0 && c.shared_inter % 64 == 0;
+  return (c.dtype == MOE_BF16 || c.dtype == MOE_F16) && c.hidden % 128 == 0 && c.inter % 64 == 0 &&
+         c.shared_inter % 64 == 0;
 }
 
 bool tc_path_supported(const moe_cfg_t& c) { return tc_shape_ok(c) && encode_fn() != nullptr; }
@@ -1053,10 +1054,9 @@ static int w2_m_tiles(int T, int k, int E, int H, int sms) {
   return (t1 + sms - 1) / sms < kMT * ((t2 + sms - 1) / sms) ? 1 : kMT;
 }
 
-template <int N>
+template <int DT, int N>
 static moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws, const WsLayout& L,
                                      int32_t T, int fused_nsplit, cudaStream_t st) {
-  constexpr int DT = MOE_BF16;
   const int H = c.hidden, E = c.n_experts, k = c.top_k, I = c.inter, Is = c.shared_inter;
   const int Imax = I > Is ? I : Is;
   const int P = static_cast<int>(L.pairs);
@@ -1220,8 +1220,12 @@ int tc_tile_n(const moe_cfg_t& c, int32_t T) {
 
 moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uint8_t* ws, const WsLayout& L, int32_t T,
                               int fused_nsplit, cudaStream_t st) {
-  if (L.tc_n == 128) return launch_tc_passes<128>(c, p, ws, L, T, fused_nsplit, st);
-  return launch_tc_passes<64>(c, p, ws, L, T, fused_nsplit, st);
+  if (c.dtype == MOE_BF16) {
+    if (L.tc_n == 128) return launch_tc_passes<MOE_BF16, 128>(c, p, ws, L, T, fused_nsplit, st);
+    return launch_tc_passes<MOE_BF16, 64>(c, p, ws, L, T, fused_nsplit, st);
+  }
+  if (L.tc_n == 128) return launch_tc_passes<MOE_F16, 128>(c, p, ws, L, T, fused_nsplit, st);
+  return launch_tc_passes<MOE_F16, 64>(c, p, ws, L, T, fused_nsplit, st);
 }
 
 }  // namespace moe

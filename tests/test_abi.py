@@ -179,11 +179,11 @@ def test_single_launch_batch_workspace(m):
     assert m.moe_workspace_bytes(c, 16) > m.moe_workspace_bytes(c, 17)
 
 
-def test_tensor_core_path_workspace_is_laid_out_for_bf16_shapes(m):
+def test_tensor_core_path_workspace_is_laid_out_for_both_dtypes(m):
     bf = m.MoeCfg(2048, 256, 8, 512, 512, m.MOE_BF16, has_shared_gate=1)
     fp = m.MoeCfg(2048, 256, 8, 512, 512, m.MOE_F16, has_shared_gate=1)
     T = 512
     P = T * 8 + T
-    extra = m.moe_workspace_bytes(bf, T) - m.moe_workspace_bytes(fp, T)
-    # gathered x rows plus the two activation terms
-    assert extra >= P * 2048 * 2 + 2 * P * 512 * 2
+    assert m.moe_workspace_bytes(bf, T) == m.moe_workspace_bytes(fp, T)
+    # fp32 activations and per-pair rows, gathered x rows and the two activation terms
+    assert m.moe_workspace_bytes(bf, T) >= P * 512 * 4 + P * 2048 * 4 + P * 2048 * 2 + 2 * P * 512 * 2

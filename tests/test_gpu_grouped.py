@@ -144,12 +144,18 @@ def test_ranked_grouping_repeats_on_one_workspace(m):
             assert torch.equal(a, b)
 
 
-def test_tcgen05_path_rejects_fp16(m):
+@pytest.mark.parametrize("T", [4, 20, 64])
+def test_tcgen05_path_fp16_sharded_shapes(m, T):
+    """fp16 weights and tokens on the tcgen05 passes (kind::f16 with fp16
+    operands, the activation split into two fp16 terms), every token against
+    the oracle at the sharded shapes (I = 128, shared I = 128)."""
     wl = moe_synth.workload("sharded_decode")
-    g = moe_synth.make_layer(wl, 0, 4, device=DEV)
-    with pytest.raises(m.MoeError) as ei:
-        _grouped(m, wl, g, 4, flags=TC)
-    assert ei.value.code == 2
+    g = moe_synth.make_layer(wl, 4, T, device=DEV)
+    m.moe_reset_stats()
+    ids, w, out = _grouped(m, wl, g, T, flags=TC)
+    assert m.moe_get_stats()["grouped_tc_calls"] == 1
+    tokens = list(range(T))
+    check_tokens(ids, w, out, oracle_tokens(wl, g, tokens), tokens, wl.top_k)
 
 
 def test_grouped_t1_dispatches_to_decode_kernel(m):
@@ -264,18 +270,17 @@ def test_no_renormalisation_no_shared_expert(m, flags):
     parity(out, ref["out"])
 
 
-def test_fp16_batches_take_the_cuda_core_path(m):
-    """fp16 with T > 16 runs the CUDA-core grouped kernels by default (the
-    tensor-core passes are bf16 only; up to 16 tokens take the single-launch
-    kernel) and matches the oracle on every token, as does an fp16 batch of 6
-    on the CUDA-core kernels."""
+def test_fp16_batches_default_to_the_tensor_core_path(m):
+    """fp16 batches run the tcgen05 passes by default from 4 tokens at these
+    shapes (I = 128) and match the oracle on every token, as does an fp16
+    batch of 6 on the CUDA-core kernels."""
     wl = moe_synth.workload("sharded_decode")
     T = 20
     g = moe_synth.make_layer(wl, 3, T, device=DEV)
     m.moe_reset_stats()
     ids, w, out = _grouped(m, wl, g, T)
     st = m.moe_get_stats()
-    assert st["grouped_calls"] == 1 and st["grouped_tc_calls"] == 0 and st["kernels_launched"] > 1
+    assert st["grouped_calls"] == 1 and st["grouped_tc_calls"] == 1 and st["kernels_launched"] > 1
     tokens = list(range(T))
     check_tokens(ids, w, out, oracle_tokens(wl, g, tokens), tokens, wl.top_k)
     T = 6
@@ -286,6 +291,16 @@ def test_fp16_batches_take_the_cuda_core_path(m):
     assert st["grouped_calls"] == 1 and st["grouped_tc_calls"] == 0
     tokens = list(range(T))
     check_tokens(ids, w, out, oracle_tokens(wl, g, tokens), tokens, wl.top_k)
+    # at I = 128 the single launch is the default up to 3 tokens, the
+    # tensor-core passes from 4
+    for T, tc in ((3, 0), (4, 1)):
+        g = moe_synth.make_layer(wl, 5, T, device=DEV)
+        m.moe_reset_stats()
+        ids, w, out = _grouped(m, wl, g, T)
+        st = m.moe_get_stats()
+        assert st["grouped_tc_calls"] == tc and (tc or st["kernels_launched"] == 1)
+        tokens = list(range(T))
+        check_tokens(ids, w, out, oracle_tokens(wl, g, tokens), tokens, wl.top_k)
 
 
 def test_zero_tokens_is_a_no_op(m):
