@@ -1170,14 +1170,15 @@ static moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uin
 
 
 bool tc_router_supported(const moe_cfg_t& c) {
-  return c.dtype == MOE_BF16 && c.hidden % 64 == 0 && encode_fn() != nullptr;
+  return (c.dtype == MOE_BF16 || c.dtype == MOE_F16) && c.hidden % 64 == 0 && encode_fn() != nullptr;
 }
 
 // logits [T, E1] (E1 = E, or E + 1 with the gate column) on tensor cores.
 moe_status_t launch_tc_router(const moe_cfg_t& c, const void* x, const void* router_w, const void* gate_w,
                               int32_t T, float* logits, float* part, int E1, Control* ctrl, cudaStream_t st,
                               int* nsplit) {
-  constexpr int DT = MOE_BF16, N = 128;
+  constexpr int N = 128;
+  const int DT = c.dtype;
   const int H = c.hidden, E = c.n_experts;
   const int mE = (E + 127) / 128;
   const int nm = mE + (gate_w ? 1 : 0);
@@ -1189,7 +1190,8 @@ moe_status_t launch_tc_router(const moe_cfg_t& c, const void* x, const void* rou
   constexpr uint32_t st_bytes = kTileA + N * 128;
   constexpr int ns = kSmemBudget / st_bytes > 8 ? 8 : kSmemBudget / st_bytes;
   const size_t smem = static_cast<size_t>(ns) * st_bytes + 1024;
-  cudaFuncSetAttribute(tc_router_kernel<DT, N>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  auto kern = DT == MOE_BF16 ? tc_router_kernel<MOE_BF16, N> : tc_router_kernel<MOE_F16, N>;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   const int tiles0 = nm * ((T + N - 1) / N);
   const int sms = sm_count();
   // K splits when the tiles would leave most SMs idle (T = 512: 12 tiles, 5.4
@@ -1206,7 +1208,7 @@ moe_status_t launch_tc_router(const moe_cfg_t& c, const void* x, const void* rou
   *nsplit = S > 1 ? S : 0;
   const int tiles = tiles0 * S;
   const int g = tiles < sms ? tiles : sms;
-  launch_pdl(tc_router_kernel<DT, N>, dim3(g), dim3(kTcThreads), smem, st, mWr, mG, mX, T, H, E, E1, mE, nm, S,
+  launch_pdl(kern, dim3(g), dim3(kTcThreads), smem, st, mWr, mG, mX, T, H, E, E1, mE, nm, S,
              S > 1 ? part : logits, ctrl, wait_timeout_ns());
   if (moe_status_t s = check_launch("tc_router_kernel")) return s;
   stat_kernels(1);

@@ -32,7 +32,7 @@ def _route(m, cfg, x, wr):
 
 
 @pytest.mark.parametrize("name,T", [("tiny", 1), ("tiny", 37), ("full_decode", 1), ("full_decode", 64),
-                                    ("chunked_prefill", 300), ("chunked_prefill", 1000)])
+                                    ("chunked_prefill", 300), ("chunked_prefill", 1000), ("sharded_decode", 300)])
 def test_router_matches_oracle(m, name, T):
     wl = moe_synth.workload(name)
     cfg = m.cfg_from_workload(wl)
