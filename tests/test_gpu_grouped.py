@@ -191,6 +191,20 @@ def test_chunked_prefill_4096_tcgen05(m):
     check_tokens(ids, w, out, _ref_tokens(wl, 0, T, g, tokens), tokens, wl.top_k)
 
 
+@pytest.mark.parametrize("T", [1023, 2049])
+def test_chunked_prefill_ragged_token_counts(m, T):
+    """Full prefill shapes at token counts with ragged tiles: 1023 (the router
+    GEMM split into K parts, the x rows copied by the filing launch) and 2049
+    (a gather launch): a seeded 128-token subset plus the first and last
+    token."""
+    wl = moe_synth.workload("chunked_prefill")
+    g = moe_synth.make_layer(wl, 1, T, device=DEV)
+    ids, w, out = _grouped(m, wl, g, T, flags=TC)
+    pick = np.random.default_rng(T).choice(np.arange(1, T - 1), 128, replace=False).tolist()
+    tokens = sorted(set([0, T - 1] + pick))
+    check_tokens(ids, w, out, _ref_tokens(wl, 1, T, g, tokens), tokens, wl.top_k)
+
+
 def test_simt_and_tcgen05_paths_agree(m):
     wl = moe_synth.workload("chunked_prefill")
     T = 300
