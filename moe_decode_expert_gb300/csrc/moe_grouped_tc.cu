@@ -829,7 +829,7 @@ __global__ void __launch_bounds__(1024) tc_fill_kernel(const int32_t* ids, const
                                                        int T, int k, int E, int has_shared, int32_t* perm, int I,
                                                        int Is, int H, int N, int mt13, int mt2, int32_t* n13,
                                                        int32_t* n2, TcTile* t13, TcTile* t2, const uint8_t* x,
-                                                       uint8_t* __restrict__ xs) {
+                                                       uint8_t* __restrict__ xs, Control* ctrl) {
   pdl_launch_dependents();  // let the next kernel on the stream launch early
   pdl_wait();               // inputs written by the previous kernel are visible
   __shared__ int32_t s_cnt[1026], s_off[1026];
@@ -865,8 +865,13 @@ __global__ void __launch_bounds__(1024) tc_fill_kernel(const int32_t* ids, const
   const int np = T * k, P = np + (has_shared ? T : 0);
   if (!xs) {
     for (int p = blockIdx.x * 1024 + tid; p < P; p += gridDim.x * 1024) {
-      if (p < np) perm[s_off[ids[p]] + rank[p]] = p;
-      else perm[s_off[E] + (p - np)] = p;
+      if (p < np) {
+        const int e = ids[p];
+        if (e >= 0 && e < E) perm[s_off[e] + rank[p]] = p;
+        else report_error(ctrl, kDevBadExpert, static_cast<uint32_t>(p));
+      } else {
+        perm[s_off[E] + (p - np)] = p;
+      }
     }
     return;
   }
@@ -874,10 +879,17 @@ __global__ void __launch_bounds__(1024) tc_fill_kernel(const int32_t* ids, const
   for (int p = blockIdx.x * 32 + warp; p < P; p += gridDim.x * 32) {
     int pos = 0;
     if (lane == 0) {
-      pos = p < np ? s_off[ids[p]] + rank[p] : s_off[E] + (p - np);
-      perm[pos] = p;
+      const int e = p < np ? ids[p] : E;
+      if (e >= 0 && e <= E) {
+        pos = p < np ? s_off[e] + rank[p] : s_off[E] + (p - np);
+        perm[pos] = p;
+      } else {
+        pos = -1;
+        report_error(ctrl, kDevBadExpert, static_cast<uint32_t>(p));
+      }
     }
     pos = __shfl_sync(0xffffffffu, pos, 0);
+    if (pos < 0) continue;
     const int t = p < np ? p / k : p - np;
     const uint8_t* src = x + static_cast<size_t>(t) * H * 2;
     uint8_t* dst = xs + static_cast<size_t>(pos) * H * 2;
@@ -1106,7 +1118,7 @@ static moe_status_t launch_tc_passes(const moe_cfg_t& c, const BlockPtrs& p, uin
     const int gf = gq < sm_count() ? gq : sm_count();
     launch_pdl(tc_fill_kernel, dim3(gf > 0 ? gf : 1), dim3(1024), 0, st, p.topk_ids, rank, cnt, T, k, E,
                Is > 0 ? 1 : 0, perm, I, Is, H, N, mt13, mt2, sched, sched + 1, t13, t2,
-               static_cast<const uint8_t*>(p.x), fold ? xs : nullptr);
+               static_cast<const uint8_t*>(p.x), fold ? xs : nullptr, ctrl);
     if (moe_status_t s = check_launch("tc_fill_kernel")) return s;
   }
   const int sms = sm_count();

@@ -260,8 +260,10 @@ __global__ void __launch_bounds__(256) router_topk_kernel(float* logits, const f
   if (t >= T) return;
   topk_token_stage<MAXM>(logits, part, nsplit, t, T, E, E1, k, norm_topk, ids, w, logits_out, s_ids[warp],
                          s_sel[warp], s_w[warp], s_row[warp]);
-  if (cnt && (threadIdx.x & 31) < k)
-    rank[static_cast<size_t>(t) * k + (threadIdx.x & 31)] = atomicAdd(&cnt[s_ids[warp][threadIdx.x & 31]], 1);
+  if (cnt && (threadIdx.x & 31) < k) {
+    const int e = s_ids[warp][threadIdx.x & 31];
+    if (e >= 0 && e < E) rank[static_cast<size_t>(t) * k + (threadIdx.x & 31)] = atomicAdd(&cnt[e], 1);
+  }
 }
 
 moe_status_t launch_router(const moe_cfg_t& c, const void* x, const void* router_w,
