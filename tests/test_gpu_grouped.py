@@ -266,12 +266,13 @@ def test_residual_flag_grouped(m, flags):
 
 
 @pytest.mark.parametrize("flags", [SIMT, TC], ids=["simt", "tcgen05"])
-def test_no_renormalisation_no_shared_expert(m, flags):
+@pytest.mark.parametrize("T", [24, 40])
+def test_no_renormalisation_no_shared_expert(m, flags, T):
     """norm_topk = 0 (full-softmax weights) and no shared expert on both T > 1
-    paths, every token against the oracle."""
+    paths, every token against the oracle (T = 40: the ranked grouping, 64
+    experts, top-6)."""
     wl = moe_synth.Workload("nonorm", 512, 64, 6, 128, 0, moe_synth.BF16, 0, 1.0, 0.05, 0.05, norm_topk=0,
                             preset_id=11)
-    T = 24
     d = moe_synth.make_layer(wl, 0, T)
     g = {k_: (v.to(DEV) if v is not None else None) for k_, v in d.items()}
     ids, w, out = _grouped(m, wl, g, T, out_dtype=3, flags=flags)
